@@ -1,0 +1,324 @@
+"""Pins that tie the CPU oracle to facts outside itself.
+
+Each pin takes the oracle library handle ``L`` so that the same checks can be
+run against deliberately mutated copies of the oracle (see
+test_oracle_mutants.py): a plausible slip anywhere in the oracle must make at
+least one pin fail.
+
+What the pins compare against (never the oracle's own formulas):
+  * PyTorch's binary32 -> bf16 conversion (round to nearest even), a library
+    routine, and hand-known bf16 bit patterns;
+  * a brute-force full Q.K^T in numpy when P is the identity (r = head_dim),
+    and when P selects coordinates (r < head_dim, P not symmetric);
+  * a hand-worked three-block example (tests/golden/hand_three_block.json);
+  * invariants: block-table permutation, exact power-of-two linearity;
+  * hand-written victim orders with ties, signed zeros, NaN and k > n.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ----------------------------------------------------------------------------- helpers
+# Conversions done by numpy / torch, never by the oracle.
+
+def to_bf16_bits(x) -> np.ndarray:
+    """float values -> bf16 bit patterns via PyTorch (round to nearest even)."""
+    t = torch.as_tensor(np.asarray(x, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def from_bf16_bits(b) -> np.ndarray:
+    """bf16 bit patterns -> float64 via numpy bit casting."""
+    b = np.asarray(b, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def bf16_normal_bits(rng: np.random.Generator, shape, std=1.0) -> np.ndarray:
+    return to_bf16_bits(rng.standard_normal(shape) * std)
+
+
+def brute_force_scores(Qv, Kv_by_id, table, seq_offsets, nkv):
+    """max over rows, heads h and tokens t of q[row,h] . k[id][t, h // g] (numpy, fp64).
+
+    Qv       [S, R, nq, e] float64 (e = the compared coordinates)
+    Kv_by_id {id: [bs, nkv, e] float64}
+    """
+    S, R, nq, _ = Qv.shape
+    g = nq // nkv
+    out = []
+    for s in range(S):
+        for i in range(int(seq_offsets[s]), int(seq_offsets[s + 1])):
+            kb = Kv_by_id[int(table[i])]
+            best = -math.inf
+            for h in range(nq):
+                # Full products of every query row of head h with every token of its kv head.
+                full = Qv[s, :, h, :] @ kb[:, h // g, :].T
+                best = max(best, float(full.max()))
+            out.append(best)
+    return np.array(out)
+
+
+# ----------------------------------------------------------------------------- bf16 rounding
+
+def pin_bf16_hand_values(L):
+    cases = [
+        (1.0, 0x3F80), (-2.0, 0xC000), (0.0, 0x0000), (-0.0, 0x8000),
+        (1.0 + 2.0 ** -8, 0x3F80),                   # tie -> even (down)
+        (1.0 + 3 * 2.0 ** -8, 0x3F82),               # tie -> even (up)
+        (1.0 + 2.0 ** -8 + 2.0 ** -40, 0x3F81),      # just above a tie: must not double-round
+        (-(1.0 + 2.0 ** -8 + 2.0 ** -40), 0xBF81),
+        (2.0 ** -127, 0x0040),                       # bf16 subnormal
+        (2.0 ** -134, 0x0000),                       # half the smallest subnormal: tie -> 0
+        (3 * 2.0 ** -134, 0x0002),                   # 1.5 spacings -> even (2)
+        (float.fromhex("0x1.FEp127"), 0x7F7F),       # largest finite
+        (float.fromhex("0x1.FFp127"), 0x7F80),       # tie above the largest: even is +inf
+        (math.inf, 0x7F80), (-math.inf, 0xFF80),
+    ]
+    got = oracle.bf16_from_double(np.array([c[0] for c in cases]), L=L)
+    exp = np.array([c[1] for c in cases], dtype=np.uint16)
+    assert np.array_equal(got, exp), (got, exp)
+    assert (oracle.bf16_from_double([math.nan], L=L)[0] & 0x7FFF) > 0x7F80
+
+
+def pin_bf16_matches_torch(L):
+    """On every binary32 input the oracle's rounding equals PyTorch's f32 -> bf16."""
+    rng = np.random.default_rng(1234)
+    bits = rng.integers(0, 2 ** 32, size=200_000, dtype=np.uint64).astype(np.uint32)
+    bits = np.concatenate([bits, np.arange(0, 70_000, dtype=np.uint32),       # subnormals
+                           np.arange(0x7F7F0000, 0x7F800000, 7, dtype=np.uint32)])  # near max
+    f = bits.view(np.float32)
+    f = f[~np.isnan(f)]
+    exp = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.bf16_from_double(f.astype(np.float64), L=L)
+    bad = np.nonzero(got != exp)[0]
+    assert bad.size == 0, f"{bad.size} mismatches, first at {f[bad[0]]!r}"
+    back = oracle.bf16_to_double(exp, L=L)
+    assert np.array_equal(back, from_bf16_bits(exp))
+
+
+# ----------------------------------------------------------------------------- method pins
+
+def _grid_case(rng, *, nq, nkv, hd, bs, S, R, lengths, layers, layer, pool):
+    total = sum(lengths)
+    ids = rng.permutation(pool)[:pool].astype(np.int32)
+    K = bf16_normal_bits(rng, (pool, bs, nkv, hd))
+    Q = bf16_normal_bits(rng, (S, R, nq, hd))
+    table = rng.permutation(pool)[:total].astype(np.int32)
+    offs = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    return Q, K, ids, table, offs
+
+
+def pin_identity_projection_brute_force(L):
+    """P = I (r = head_dim): Qp = Q and A_g = K exactly; scores = max of the full Q.K^T."""
+    rng = np.random.default_rng(7)
+    nq, nkv, hd, bs, S, R = 4, 2, 64, 16, 2, 3
+    lengths, layers, layer, pool = [5, 9], 3, 2, 16
+    Q, K, ids, table, offs = _grid_case(rng, nq=nq, nkv=nkv, hd=hd, bs=bs, S=S, R=R,
+                                        lengths=lengths, layers=layers, layer=layer, pool=pool)
+    P = to_bf16_bits(np.eye(hd))
+    Qp = oracle.project_q(Q, P, L=L)
+    assert np.array_equal(Qp, Q)
+    A = np.zeros((layers, pool, nkv, bs, hd), dtype=np.uint16)
+    assert oracle.project_kv_blocks(P, K, layer, ids, A, L=L) == 0
+    for i, bid in enumerate(ids):
+        assert np.array_equal(A[layer, bid], K[i].transpose(1, 0, 2)), "slot != K^T"
+    assert not A[:layer].any() and not A[layer + 1:].any(), "wrote another layer"
+    score, tsum, bad = oracle.score_blocks(Qp, A, layer, table, offs, L=L)
+    assert bad == 0
+    Kd = {int(bid): from_bf16_bits(K[i]) for i, bid in enumerate(ids)}
+    exp = brute_force_scores(from_bf16_bits(Q), Kd, table, offs, nkv)
+    assert np.array_equal(score, exp), np.max(np.abs(score - exp))
+    assert np.all(tsum >= np.abs(score))
+
+
+def pin_selection_projection_brute_force(L):
+    """P selects r of head_dim coordinates (times 2): a non-symmetric, non-square P."""
+    rng = np.random.default_rng(11)
+    nq, nkv, hd, r, bs, S, R = 6, 3, 48, 16, 4, 3, 2
+    lengths, layers, layer, pool = [4, 1, 6], 2, 1, 12
+    Q, K, ids, table, offs = _grid_case(rng, nq=nq, nkv=nkv, hd=hd, bs=bs, S=S, R=R,
+                                        lengths=lengths, layers=layers, layer=layer, pool=pool)
+    sel = rng.permutation(hd)[:r]
+    Pf = np.zeros((hd, r))
+    Pf[sel, np.arange(r)] = 2.0
+    P = to_bf16_bits(Pf)
+    Qp = oracle.project_q(Q, P, L=L)
+    assert np.array_equal(from_bf16_bits(Qp), 2.0 * from_bf16_bits(Q)[..., sel])
+    A = np.zeros((layers, pool, nkv, bs, r), dtype=np.uint16)
+    assert oracle.project_kv_blocks(P, K, layer, ids, A, L=L) == 0
+    Kf = from_bf16_bits(K)
+    for i, bid in enumerate(ids):
+        assert np.array_equal(from_bf16_bits(A[layer, bid]),
+                              2.0 * Kf[i][..., sel].transpose(1, 0, 2))
+    score, _, bad = oracle.score_blocks(Qp, A, layer, table, offs, L=L)
+    Kd = {int(bid): 2.0 * Kf[i][..., sel] for i, bid in enumerate(ids)}
+    exp = brute_force_scores(2.0 * from_bf16_bits(Q)[..., sel], Kd, table, offs, nkv)
+    assert bad == 0 and np.array_equal(score, exp)
+
+
+def pin_gqa_contiguous_groups(L):
+    """Query head h reads kv head h // g: a case where h % nkv would give another score."""
+    nq, nkv, hd, bs = 4, 2, 16, 16
+    P = to_bf16_bits(np.eye(hd))
+    Q = np.zeros((1, 1, nq, hd))
+    Q[0, 0, 2, 0] = Q[0, 0, 3, 0] = 1.0         # heads 2, 3 (group of kv head 1)
+    K = np.zeros((1, bs, nkv, hd))
+    K[0, :, 0, 0] = 4.0                         # kv head 0: large, read only by heads 0, 1
+    K[0, 5, 1, 0] = 1.0                         # kv head 1: one token with a 1
+    A = np.zeros((1, 1, nkv, bs, hd), dtype=np.uint16)
+    oracle.project_kv_blocks(P, to_bf16_bits(K), 0, np.array([0]), A, L=L)
+    score, _, _ = oracle.score_blocks(oracle.project_q(to_bf16_bits(Q), P, L=L), A, 0,
+                                      np.array([0]), np.array([0, 1]), L=L)
+    assert score[0] == 1.0, score
+
+
+def pin_hand_example(L):
+    g = json.load(open(os.path.join(GOLDEN, "hand_three_block.json")))
+    d = g["dims"]
+    P = to_bf16_bits(g["P"])
+    Q = to_bf16_bits(np.array(g["Q"], dtype=np.float64).reshape(1, 1, d["num_q_heads"],
+                                                                  d["head_dim"]))
+    K = to_bf16_bits(g["K"])
+    Qp = oracle.project_q(Q, P, L=L)
+    assert np.array_equal(from_bf16_bits(Qp).reshape(d["num_q_heads"], d["r"]),
+                          np.array(g["expected_Qp"], dtype=np.float64))
+    A = np.zeros((1, d["max_blocks"], d["num_kv_heads"], d["block_size"], d["r"]),
+                 dtype=np.uint16)
+    assert oracle.project_kv_blocks(P, K, 0, np.arange(d["max_blocks"]), A, L=L) == 0
+    assert np.array_equal(from_bf16_bits(A[0]), np.array(g["expected_A_g_slots"]))
+    for c in g["cases"]:
+        offs = np.array(c["seq_offsets"])
+        S = len(offs) - 1
+        QpS = np.repeat(Qp, S, axis=0)
+        score, _, bad = oracle.score_blocks(QpS, A, 0, np.array(c["table"]), offs, L=L)
+        assert bad == 0 and np.array_equal(score, np.array(c["expected_scores"], dtype=float))
+        vic = oracle.rank_victims(score.astype(np.float32), offs, c["k"], L=L)
+        assert np.array_equal(vic, np.array(c["expected_victims"])), (vic, c)
+
+
+def pin_table_permutation(L):
+    """Permuting a sequence's table permutes its scores the same way."""
+    rng = np.random.default_rng(5)
+    nq, nkv, hd, r, bs, pool = 8, 2, 32, 16, 16, 40
+    P = bf16_normal_bits(rng, (hd, r), std=1 / math.sqrt(r))
+    K = bf16_normal_bits(rng, (pool, bs, nkv, hd))
+    Q = bf16_normal_bits(rng, (2, 2, nq, hd))
+    A = np.zeros((1, pool, nkv, bs, r), dtype=np.uint16)
+    oracle.project_kv_blocks(P, K, 0, np.arange(pool), A, L=L)
+    Qp = oracle.project_q(Q, P, L=L)
+    table = rng.permutation(pool)[:30].astype(np.int32)
+    offs = np.array([0, 13, 30])
+    base, _, _ = oracle.score_blocks(Qp, A, 0, table, offs, L=L)
+    perm = np.concatenate([rng.permutation(13), 13 + rng.permutation(17)])
+    moved, _, _ = oracle.score_blocks(Qp, A, 0, table[perm], offs, L=L)
+    assert np.array_equal(moved, base[perm])
+    k = 6
+    v0 = oracle.rank_victims(base.astype(np.float32), offs, k, L=L)
+    v1 = oracle.rank_victims(moved.astype(np.float32), offs, k, L=L)
+    for s in range(2):
+        a, b = offs[s], offs[s + 1]
+        # The permuted table's victim j is entry perm[a + j] of the original table.
+        mapped = perm[a + v1[s]] - a
+        assert sorted(mapped.tolist()) == sorted(v0[s].tolist())
+
+
+def pin_linearity(L):
+    """Doubling K doubles A_g exactly; doubling Q doubles Qp; scores scale by 2 and 4."""
+    rng = np.random.default_rng(9)
+    nq, nkv, hd, r, bs, pool = 4, 2, 32, 16, 16, 8
+    P = bf16_normal_bits(rng, (hd, r), std=1 / math.sqrt(r))
+    K = bf16_normal_bits(rng, (pool, bs, nkv, hd))
+    Q = bf16_normal_bits(rng, (1, 1, nq, hd))
+    K2 = to_bf16_bits(2.0 * from_bf16_bits(K))
+    Q2 = to_bf16_bits(2.0 * from_bf16_bits(Q))
+    A1 = np.zeros((1, pool, nkv, bs, r), dtype=np.uint16)
+    A2 = np.zeros_like(A1)
+    oracle.project_kv_blocks(P, K, 0, np.arange(pool), A1, L=L)
+    oracle.project_kv_blocks(P, K2, 0, np.arange(pool), A2, L=L)
+    assert np.array_equal(from_bf16_bits(A2), 2.0 * from_bf16_bits(A1))
+    q1 = oracle.project_q(Q, P, L=L)
+    q2 = oracle.project_q(Q2, P, L=L)
+    assert np.array_equal(from_bf16_bits(q2), 2.0 * from_bf16_bits(q1))
+    t, offs = np.arange(pool), np.array([0, pool])
+    s11, _, _ = oracle.score_blocks(q1, A1, 0, t, offs, L=L)
+    s12, _, _ = oracle.score_blocks(q1, A2, 0, t, offs, L=L)
+    s22, _, _ = oracle.score_blocks(q2, A2, 0, t, offs, L=L)
+    assert np.array_equal(s12, 2.0 * s11) and np.array_equal(s22, 4.0 * s11)
+
+
+def pin_out_of_range(L):
+    """Bad layer: nothing written; bad block id: skipped, reported, scored +inf."""
+    rng = np.random.default_rng(3)
+    P = bf16_normal_bits(rng, (16, 16))
+    K = bf16_normal_bits(rng, (3, 16, 1, 16))
+    A = np.zeros((2, 4, 1, 16, 16), dtype=np.uint16)
+    assert oracle.project_kv_blocks(P, K, 2, np.array([0, 1, 2]), A, L=L) == -1
+    assert not A.any()
+    assert oracle.project_kv_blocks(P, K, 1, np.array([0, 4, 2]), A, L=L) == 2
+    assert A[1, 0].any() and A[1, 2].any() and not A[1, 1].any() and not A[0].any()
+    Qp = bf16_normal_bits(rng, (1, 1, 1, 16))
+    score, tsum, bad = oracle.score_blocks(Qp, A, 1, np.array([0, -1, 4, 2]),
+                                           np.array([0, 4]), L=L)
+    assert bad == 2 and math.isinf(score[1]) and math.isinf(score[2])
+    assert np.isfinite(score[[0, 3]]).all() and tsum[1] == 0.0
+
+
+def pin_victim_order(L):
+    """Hand-written victim orders: ties, signed zeros, NaN, +-inf, k > n, empty sequences."""
+    nan, inf = math.nan, math.inf
+    scores = np.array([
+        3.0, 1.0, 1.0, -2.0, 0.0, -0.0, 5.0,      # seq 0 (7 entries)
+        nan, inf, -inf, 2.0,                       # seq 1 (4 entries)
+                                                   # seq 2 (empty)
+        0.5, 0.5, 0.5,                             # seq 3 (3 entries)
+    ], dtype=np.float32)
+    offs = np.array([0, 7, 11, 11, 14])
+    k = 5
+    exp = np.array([
+        [3, 4, 5, 1, 2],           # -2, then 0 / -0 (equal: lower index first), then 1, 1
+        [2, 3, 0, 1, -1],          # -inf, 2, NaN (as +inf, index 0) before +inf (index 1)
+        [-1, -1, -1, -1, -1],
+        [0, 1, 2, -1, -1],
+    ])
+    got = oracle.rank_victims(scores, offs, k, L=L)
+    assert np.array_equal(got, exp), got
+
+
+def pin_victims_brute_force(L):
+    """Victims equal a plain Python sort of (score, index) on random data with ties."""
+    rng = np.random.default_rng(21)
+    lengths = [0, 1, 17, 64, 300]
+    offs = np.concatenate([[0], np.cumsum(lengths)])
+    s = np.round(rng.standard_normal(offs[-1]) * 4).astype(np.float32)  # many exact ties
+    k = 20
+    got = oracle.rank_victims(s, offs, k, L=L)
+    for si in range(len(lengths)):
+        seg = s[offs[si]:offs[si + 1]]
+        order = sorted(range(len(seg)), key=lambda i: (float(seg[i]), i))[:k]
+        exp = order + [-1] * (k - len(order))
+        assert got[si].tolist() == exp
+
+
+ALL_PINS = [
+    pin_bf16_hand_values,
+    pin_bf16_matches_torch,
+    pin_identity_projection_brute_force,
+    pin_selection_projection_brute_force,
+    pin_gqa_contiguous_groups,
+    pin_hand_example,
+    pin_table_permutation,
+    pin_linearity,
+    pin_out_of_range,
+    pin_victim_order,
+    pin_victims_brute_force,
+]

@@ -1,0 +1,91 @@
+"""Each plausible slip planted in a copy of the oracle must fail at least one pin.
+
+The mutants are made on the CPU from the oracle's source text at test time:
+a dropped term, a wrong index, a transposed operand, a wrong sign, a wrong
+rounding, a broken tie-break.  The committed oracle itself is never changed.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import oracle_pins as pins
+
+SRC = open(os.path.join(os.path.dirname(oracle.__file__), "hss_oracle.c")).read()
+
+# (name, text to replace, replacement, which occurrence (0-based)).
+# Not listed: loosening the explicit overflow test in the bf16 rounding, which
+# is an equivalent mutant (the binary32 conversion of 2^128 is +inf anyway).
+MUTANTS = [
+    ("q_drops_first_term", "for (int d = 0; d < k->hd; ++d) {\n            acc +=",
+     "for (int d = 1; d < k->hd; ++d) {\n            acc +=", 0),
+    ("kv_drops_last_term", "for (int d = 0; d < k->hd; ++d) {\n                    acc +=",
+     "for (int d = 0; d + 1 < k->hd; ++d) {\n                    acc +=", 0),
+    ("q_transposed_P", "k->P[(int64_t)d * k->r + j]", "k->P[(int64_t)j * k->hd + d]", 0),
+    ("kv_transposed_P", "k->P[(int64_t)d * k->r + j]", "k->P[(int64_t)j * k->hd + d]", 1),
+    ("slot_not_transposed", "slot[((int64_t)h * k->bs + t) * k->r + j]",
+     "slot[((int64_t)t * k->nkv + h) * k->r + j]", 0),
+    ("kv_input_head_major", "kb + ((int64_t)t * k->nkv + h) * k->hd",
+     "kb + ((int64_t)h * k->bs + t) * k->hd", 0),
+    ("gqa_modulo", "int c_kv = h / g;", "int c_kv = h % k->nkv;", 0),
+    ("score_ignores_layer", "k->A + (k->layer * k->max_blocks + id) * slot_elems;\n    double best",
+     "k->A + (id) * slot_elems;\n    double best", 0),
+    ("kv_ignores_layer", "k->A + (k->layer * k->max_blocks + id) * slot_elems;\n    const uint16_t* kb",
+     "k->A + (id) * slot_elems;\n    const uint16_t* kb", 0),
+    ("score_wrong_row_index", "((s * k->rows + row) * (int64_t)k->nq + h)",
+     "((s + row) * (int64_t)k->nq + h)", 0),
+    ("score_max_floor_zero", "double best = -INFINITY;", "double best = 0.0;", 0),
+    ("score_min_not_max", "if (dot > best) {", "if (-dot > -best || best == -INFINITY) {", 0),
+    ("score_abs_dot", "dot += term;", "dot += fabs(term);", 0),
+    ("round_toward_zero", "double q = nearbyint(ldexp(x, -qexp));",
+     "double q = trunc(ldexp(x, -qexp));", 0),
+    ("round_half_away", "double q = nearbyint(ldexp(x, -qexp));",
+     "double q = round(ldexp(x, -qexp));", 0),
+    ("double_rounding", "double q = nearbyint(ldexp(x, -qexp));",
+     "double q = nearbyint(ldexp((double)(float)x, -qexp));", 0),
+    ("seven_bits_only", "int qexp = e - 8;", "int qexp = e - 7;", 0),
+    ("no_subnormal_floor", "if (qexp < -133) {\n            qexp = -133;",
+     "if (qexp < -149) {\n            qexp = -149;", 0),
+    ("tie_break_reversed", "return (x->idx > y->idx) - (x->idx < y->idx);",
+     "return (x->idx < y->idx) - (x->idx > y->idx);", 0),
+    ("descending_victims", "if (x->v < y->v) {\n        return -1;",
+     "if (x->v > y->v) {\n        return -1;", 0),
+    ("nan_not_mapped", "if (isnan(v)) {\n                v = INFINITY;",
+     "if (isnan(v)) {\n                v = -INFINITY;", 0),
+    ("no_minus_one_pad", "victims[s * (int64_t)k + j] = j < n ? keyed[j].idx : -1;",
+     "victims[s * (int64_t)k + j] = j < n ? keyed[j].idx : 0;", 0),
+    ("bad_id_scored_zero", "*score = INFINITY;\n        *tsum = 0.0;",
+     "*score = 0.0;\n        *tsum = 0.0;", 0),
+]
+
+
+def _mutate(text, old, new, occurrence):
+    pos = -1
+    for _ in range(occurrence + 1):
+        pos = text.find(old, pos + 1)
+        assert pos >= 0, f"mutation site not found: {old!r}"
+    return text[:pos] + new + text[pos + len(old):]
+
+
+@pytest.mark.parametrize("name,old,new,occ", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, old, new, occ, tmp_path):
+    src = tmp_path / f"{name}.c"
+    src.write_text(_mutate(SRC, old, new, occ))
+    so = oracle.build(force=True, src=str(src), out=str(tmp_path / f"lib{name}.so"))
+    L = oracle.load_from(so)
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(L)
+        except Exception as e:  # an assertion, or a crash-free error raised by the pin
+            caught.append((pin.__name__, type(e).__name__))
+    assert caught, f"mutant {name} passed every pin"
+
+
+def test_unmutated_copy_passes(tmp_path):
+    src = tmp_path / "same.c"
+    src.write_text(SRC)
+    L = oracle.load_from(oracle.build(force=True, src=str(src), out=str(tmp_path / "libsame.so")))
+    for pin in pins.ALL_PINS:
+        pin(L)
