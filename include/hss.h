@@ -1,0 +1,194 @@
+/*
+ * hss.h -- C ABI of the GB300 (sm_103a) low-rank KV-block predictor.
+ *
+ * The predictor ("high-speed swap" block predictor, page
+ * "metrale_storage/predictor.rs", module docs) keeps, for every key token of
+ * every paged KV block, a low-rank copy of the key:
+ *
+ *     A_g[layer][block][kv_head][token][j] = bf16( sum_d K[token][kv_head][d] * P[d][j] )
+ *
+ * and scores each block against the current queries as the largest projected
+ * dot product Qp . A_g over query heads, query rows and the block's tokens.
+ * The lowest-scoring blocks are the eviction victims.
+ *
+ * Conventions for every call:
+ *   - bf16 tensors are passed as uint16_t bit patterns (IEEE binary32 upper
+ *     halves); every tensor is dense, row-major, in the layout stated.
+ *   - Pointers marked "device" must point to memory of the current CUDA
+ *     device; the caller owns every buffer.  The library allocates no memory
+ *     and keeps no state between calls other than the per-device kernel set-up
+ *     done on first use and one device-resident error word (see
+ *     hss_read_device_error).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     compute call only validates its arguments on the host and enqueues work
+ *     on that stream; it returns before the work is done.  Nothing is enqueued
+ *     when a call returns an error.
+ *   - Argument errors are reported synchronously by the return value.  Errors
+ *     that depend on device-resident data (a block id out of range) are
+ *     reported through the optional `dev_status` word (device int32): the
+ *     kernel stores the first error code into it if it is still HSS_OK; the
+ *     caller zeroes it before the call and reads it after synchronising.
+ */
+#ifndef HSS_H
+#define HSS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The seven predictor dimensions (PredictorDims on the predictor page).
+ * num_q_heads must be a multiple of num_kv_heads (PredictorDims::validate);
+ * query head h reads kv head h / (num_q_heads / num_kv_heads).
+ * Shapes the kernels support: head_dim in {16, 32, 64, 128, 192, 256};
+ * r a multiple of 16 in [16, 256]; block_size a multiple of 16 in [16, 256];
+ * num_kv_heads <= 64; max_blocks <= 2^31 - 1. */
+typedef struct hss_dims {
+    int32_t num_layers;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t r;
+    int32_t block_size;
+    int64_t max_blocks;
+} hss_dims;
+
+typedef enum hss_status {
+    HSS_OK = 0,
+    HSS_ERR_INVALID_DIMS = 1,        /* a dimension is <= 0, or num_q_heads % num_kv_heads != 0 */
+    HSS_ERR_OUT_OF_RANGE = 2,        /* layer >= num_layers, or a block id outside [0, max_blocks) */
+    HSS_ERR_NULL_POINTER = 3,        /* a required pointer is NULL */
+    HSS_ERR_MISALIGNED = 4,          /* a bf16 tensor is not 16-byte aligned */
+    HSS_ERR_WORKSPACE_TOO_SMALL = 5, /* reserved for calls that take a workspace */
+    HSS_ERR_UNSUPPORTED_SHAPE = 6,   /* valid dims that no kernel here handles */
+    HSS_ERR_CUDA = 7,                /* a CUDA runtime call or a launch failed */
+    HSS_ERR_DEVICE_TIMEOUT = 8,      /* a kernel gave up waiting on a pipeline barrier */
+    HSS_ERR_INVALID_ARGUMENT = 9     /* a count or size is negative or inconsistent */
+} hss_status;
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* hss_status_string(int32_t status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t hss_version(void);
+
+/* HSS_OK if the dims are valid (PredictorDims::validate) and supported. */
+hss_status hss_validate_dims(const hss_dims* dims);
+
+/* Bytes of the per-token low-rank key store A_g,
+ * num_layers * max_blocks * num_kv_heads * block_size * r * 2
+ * (PredictorDims::a_g_bytes, predictor page); 0 if dims is NULL or invalid. */
+size_t hss_a_g_bytes(const hss_dims* dims);
+
+/*
+ * Query projection: Qp = Q . P, rounded once to bf16 (round to nearest even).
+ * Page "metrale_storage/predictor.rs", Predictor::project_q ("q_proj = q @ P";
+ * q is [num_q_heads, head_dim] BF16, q_proj [num_q_heads, r] BF16), extended
+ * here to many query rows.
+ *
+ *   P    device, [head_dim, r] bf16, 16-byte aligned
+ *   Q    device, [num_rows, num_q_heads, head_dim] bf16, 16-byte aligned
+ *   Qp   device, [num_rows, num_q_heads, r] bf16, 16-byte aligned (output)
+ *   num_rows >= 0 query rows (num_rows = 0 enqueues nothing)
+ * Accumulation is fp32 on the tensor cores.
+ */
+hss_status hss_project_q(const hss_dims* dims, const uint16_t* P, const uint16_t* Q,
+                         int64_t num_rows, uint16_t* Qp, void* stream);
+
+/*
+ * Key projection of whole blocks into A_g:
+ *   A_g[layer][block_ids[i]][h][t][j] = bf16( sum_d K[i][t][h][d] * P[d][j] ).
+ * Page "metrale_storage/predictor.rs", Predictor::project_kv_block (k_block is
+ * [block_size, num_kv_heads, head_dim] BF16, token-major; the A_g slot is
+ * [num_kv_heads, block_size, r], head-major; an out-of-range layer or block
+ * is an error), batched here over num_blocks blocks per call.
+ *
+ *   P          device, [head_dim, r] bf16, 16-byte aligned
+ *   K          device, [num_blocks, block_size, num_kv_heads, head_dim] bf16,
+ *              16-byte aligned
+ *   layer      0 <= layer < num_layers, else HSS_ERR_OUT_OF_RANGE
+ *   block_ids  device, [num_blocks] int32; ids should be distinct (two
+ *              entries with the same id race for the slot).  An id outside
+ *              [0, max_blocks) is skipped and sets *dev_status to
+ *              HSS_ERR_OUT_OF_RANGE.
+ *   A_g        device, [num_layers, max_blocks, num_kv_heads, block_size, r]
+ *              bf16, 16-byte aligned; only the addressed slots are written
+ *   dev_status device int32 or NULL
+ */
+hss_status hss_project_kv_blocks(const hss_dims* dims, const uint16_t* P, const uint16_t* K,
+                                 int32_t layer, const int32_t* block_ids, int64_t num_blocks,
+                                 uint16_t* A_g, int32_t* dev_status, void* stream);
+
+/* Score kernel choice for hss_score_blocks. */
+#define HSS_PATH_AUTO 0    /* decode kernel when rows_per_seq * (num_q_heads/num_kv_heads) <= 16,
+                              else the tensor-memory (tcgen05) kernel */
+#define HSS_PATH_DECODE 1  /* streaming kernel: warp-level MMA per block, A_g read once */
+#define HSS_PATH_TCGEN05 2 /* dense kernel for prefill chunks: tcgen05 MMA, TMEM accumulators */
+
+/*
+ * Block scores:
+ *   scores[i] = max over query rows, query heads h and tokens t of block
+ *               block_table[i] of  sum_j Qp[s][row][h][j] * A_g[layer][block_table[i]][h/g][t][j]
+ * for i in sequence s (seq_offsets[s] <= i < seq_offsets[s+1]), g =
+ * num_q_heads / num_kv_heads.  No scaling, no masking: every token of the
+ * block is scored.  Page "metrale_storage/predictor.rs",
+ * Predictor::score_blocks (the max over query heads and tokens of the
+ * projected dot product, f32 out); that call scores contiguous slots, which
+ * an identity table reproduces.
+ *
+ *   Qp           device, [num_seqs, rows_per_seq, num_q_heads, r] bf16,
+ *                16-byte aligned
+ *   rows_per_seq >= 1 query rows per sequence
+ *   A_g          device, as in hss_project_kv_blocks
+ *   block_table  device, [total_blocks] int32 physical block ids
+ *   seq_offsets  device, [num_seqs + 1] int32, non-decreasing,
+ *                seq_offsets[0] = 0, seq_offsets[num_seqs] = total_blocks
+ *   scores       device, [total_blocks] f32 (output)
+ *   path         HSS_PATH_*
+ *   dev_status   device int32 or NULL.  A table entry outside
+ *                [0, max_blocks) gets score +inf (so it is never a victim)
+ *                and sets HSS_ERR_OUT_OF_RANGE.
+ * Accumulation is fp32; the result differs from an exact sum by at most
+ * about r * 2^-23 * sum_j |Qp_j * A_j|.
+ */
+hss_status hss_score_blocks(const hss_dims* dims, const uint16_t* Qp, int32_t rows_per_seq,
+                            const uint16_t* A_g, int32_t layer, const int32_t* block_table,
+                            const int32_t* seq_offsets, int32_t num_seqs, int64_t total_blocks,
+                            float* scores, int32_t path, int32_t* dev_status, void* stream);
+
+/* Largest k that hss_rank_victims accepts. */
+#define HSS_MAX_VICTIMS 8192
+
+/*
+ * Eviction victims: for each sequence s, the min(k, n_s) table entries with
+ * the smallest scores, in ascending order of (score, entry index), written as
+ * indices into that sequence's own table (0 .. n_s - 1); the rest of the row
+ * is -1.  -0 ranks equal to +0; NaN ranks as +inf.  The predictor page says
+ * the scores serve only to rank eviction victims (module docs of
+ * "metrale_storage/predictor.rs"); the lower-index-first rule for equal scores
+ * mirrors the host top-k of "metrale_model_layers/layers/qsa_select.rs".
+ *
+ *   scores       device, [total_blocks] f32
+ *   seq_offsets  device, [num_seqs + 1] int32, as in hss_score_blocks
+ *   k            1 <= k <= HSS_MAX_VICTIMS
+ *   victims      device, [num_seqs, k] int32 (output)
+ * The result is exact (integer output, no tolerance).
+ */
+hss_status hss_rank_victims(const float* scores, const int32_t* seq_offsets, int32_t num_seqs,
+                            int64_t total_blocks, int32_t k, int32_t* victims, void* stream);
+
+/*
+ * Device-side error word of the current device: the first HSS_ERR_* code a
+ * kernel raised since the last read (HSS_ERR_DEVICE_TIMEOUT when a pipeline
+ * wait ran out), or HSS_OK.  Synchronises `stream`, copies the word to
+ * *status and clears it.
+ */
+hss_status hss_read_device_error(int32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HSS_H */

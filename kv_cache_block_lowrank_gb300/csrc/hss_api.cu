@@ -1,0 +1,216 @@
+// hss_api.cu -- the C ABI (include/hss.h): host-side validation, per-device set-up and
+// dispatch to the kernels.  Every check runs before anything is enqueued, so a call that
+// returns an error has launched nothing.
+#include <mutex>
+
+#include "internal.h"
+
+namespace hss {
+namespace {
+
+// The library's own device error word (one per device that loads the library).
+__device__ int32_t g_device_error = 0;
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_info[kMaxDevices];
+bool g_info_ready[kMaxDevices] = {false};
+std::mutex g_info_mu;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+const DeviceInfo* current_device_info() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_info_mu);
+    if (!g_info_ready[dev]) {
+        DeviceInfo info;
+        info.device = dev;
+        if (cudaDeviceGetAttribute(&info.num_sms, cudaDevAttrMultiProcessorCount, dev) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&info.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                   dev) != cudaSuccess) {
+            return nullptr;
+        }
+        void* addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess) return nullptr;
+        info.error_word = static_cast<int32_t*>(addr);
+        g_info[dev] = info;
+        g_info_ready[dev] = true;
+    }
+    return &g_info[dev];
+}
+
+static hss_status check_dims(const hss_dims* d) {
+    if (d == nullptr) return HSS_ERR_NULL_POINTER;
+    if (d->num_layers <= 0 || d->num_q_heads <= 0 || d->num_kv_heads <= 0 || d->head_dim <= 0 ||
+        d->r <= 0 || d->block_size <= 0 || d->max_blocks <= 0)
+        return HSS_ERR_INVALID_DIMS;
+    if (d->num_q_heads % d->num_kv_heads != 0) return HSS_ERR_INVALID_DIMS;
+    if (d->max_blocks > 0x7FFFFFFF) return HSS_ERR_UNSUPPORTED_SHAPE;
+    if (d->num_kv_heads > 64) return HSS_ERR_UNSUPPORTED_SHAPE;
+    if (d->r % 16 != 0 || d->r > 256) return HSS_ERR_UNSUPPORTED_SHAPE;
+    if (d->block_size % 16 != 0 || d->block_size > 256) return HSS_ERR_UNSUPPORTED_SHAPE;
+    if (d->head_dim % 64 != 0 || d->head_dim > 256) return HSS_ERR_UNSUPPORTED_SHAPE;
+    return HSS_OK;
+}
+
+}  // namespace hss
+
+using namespace hss;
+
+extern "C" {
+
+const char* hss_status_string(int32_t status) {
+    switch (status) {
+        case HSS_OK: return "HSS_OK";
+        case HSS_ERR_INVALID_DIMS: return "HSS_ERR_INVALID_DIMS";
+        case HSS_ERR_OUT_OF_RANGE: return "HSS_ERR_OUT_OF_RANGE";
+        case HSS_ERR_NULL_POINTER: return "HSS_ERR_NULL_POINTER";
+        case HSS_ERR_MISALIGNED: return "HSS_ERR_MISALIGNED";
+        case HSS_ERR_WORKSPACE_TOO_SMALL: return "HSS_ERR_WORKSPACE_TOO_SMALL";
+        case HSS_ERR_UNSUPPORTED_SHAPE: return "HSS_ERR_UNSUPPORTED_SHAPE";
+        case HSS_ERR_CUDA: return "HSS_ERR_CUDA";
+        case HSS_ERR_DEVICE_TIMEOUT: return "HSS_ERR_DEVICE_TIMEOUT";
+        case HSS_ERR_INVALID_ARGUMENT: return "HSS_ERR_INVALID_ARGUMENT";
+        default: return "HSS_ERR_UNKNOWN";
+    }
+}
+
+int32_t hss_version(void) { return 100; }
+
+hss_status hss_validate_dims(const hss_dims* dims) { return check_dims(dims); }
+
+size_t hss_a_g_bytes(const hss_dims* d) {
+    if (d == nullptr || d->num_layers <= 0 || d->num_q_heads <= 0 || d->num_kv_heads <= 0 ||
+        d->head_dim <= 0 || d->r <= 0 || d->block_size <= 0 || d->max_blocks <= 0 ||
+        d->num_q_heads % d->num_kv_heads != 0)
+        return 0;
+    return static_cast<size_t>(d->num_layers) * static_cast<size_t>(d->max_blocks) *
+           static_cast<size_t>(d->num_kv_heads) * static_cast<size_t>(d->block_size) *
+           static_cast<size_t>(d->r) * 2u;
+}
+
+hss_status hss_project_q(const hss_dims* dims, const uint16_t* P, const uint16_t* Q,
+                         int64_t num_rows, uint16_t* Qp, void* stream) {
+    hss_status st = check_dims(dims);
+    if (st != HSS_OK) return st;
+    if (num_rows < 0) return HSS_ERR_INVALID_ARGUMENT;
+    if (num_rows == 0) return HSS_OK;
+    if (P == nullptr || Q == nullptr || Qp == nullptr) return HSS_ERR_NULL_POINTER;
+    if (!aligned16(P) || !aligned16(Q) || !aligned16(Qp)) return HSS_ERR_MISALIGNED;
+    if (num_rows > (int64_t{1} << 40) / dims->num_q_heads) return HSS_ERR_INVALID_ARGUMENT;
+    ProjectArgs a{};
+    a.P = P;
+    a.X = Q;
+    a.num_rows = num_rows * dims->num_q_heads;
+    a.head_dim = dims->head_dim;
+    a.r = dims->r;
+    a.out = Qp;
+    a.block_ids = nullptr;
+    return launch_project(a, static_cast<cudaStream_t>(stream));
+}
+
+hss_status hss_project_kv_blocks(const hss_dims* dims, const uint16_t* P, const uint16_t* K,
+                                 int32_t layer, const int32_t* block_ids, int64_t num_blocks,
+                                 uint16_t* A_g, int32_t* dev_status, void* stream) {
+    hss_status st = check_dims(dims);
+    if (st != HSS_OK) return st;
+    if (layer < 0 || layer >= dims->num_layers) return HSS_ERR_OUT_OF_RANGE;
+    if (num_blocks < 0) return HSS_ERR_INVALID_ARGUMENT;
+    if (num_blocks == 0) return HSS_OK;
+    if (P == nullptr || K == nullptr || block_ids == nullptr || A_g == nullptr)
+        return HSS_ERR_NULL_POINTER;
+    if (!aligned16(P) || !aligned16(K) || !aligned16(A_g)) return HSS_ERR_MISALIGNED;
+    const int64_t rows_per_block = static_cast<int64_t>(dims->block_size) * dims->num_kv_heads;
+    if (num_blocks > (int64_t{1} << 31) / rows_per_block) return HSS_ERR_INVALID_ARGUMENT;
+    ProjectArgs a{};
+    a.P = P;
+    a.X = K;
+    a.num_rows = num_blocks * rows_per_block;
+    a.head_dim = dims->head_dim;
+    a.r = dims->r;
+    a.out = A_g;
+    a.block_ids = block_ids;
+    a.num_kv_heads = dims->num_kv_heads;
+    a.block_size = dims->block_size;
+    a.max_blocks = dims->max_blocks;
+    a.layer = layer;
+    a.dev_status = dev_status;
+    return launch_project(a, static_cast<cudaStream_t>(stream));
+}
+
+hss_status hss_score_blocks(const hss_dims* dims, const uint16_t* Qp, int32_t rows_per_seq,
+                            const uint16_t* A_g, int32_t layer, const int32_t* block_table,
+                            const int32_t* seq_offsets, int32_t num_seqs, int64_t total_blocks,
+                            float* scores, int32_t path, int32_t* dev_status, void* stream) {
+    hss_status st = check_dims(dims);
+    if (st != HSS_OK) return st;
+    if (layer < 0 || layer >= dims->num_layers) return HSS_ERR_OUT_OF_RANGE;
+    if (num_seqs < 0 || total_blocks < 0 || rows_per_seq < 1 || total_blocks > 0x7FFFFFFF)
+        return HSS_ERR_INVALID_ARGUMENT;
+    if (path != HSS_PATH_AUTO && path != HSS_PATH_DECODE && path != HSS_PATH_TCGEN05)
+        return HSS_ERR_INVALID_ARGUMENT;
+    if (num_seqs == 0 && total_blocks != 0) return HSS_ERR_INVALID_ARGUMENT;
+    if (total_blocks == 0) return HSS_OK;
+    if (Qp == nullptr || A_g == nullptr || block_table == nullptr || seq_offsets == nullptr ||
+        scores == nullptr)
+        return HSS_ERR_NULL_POINTER;
+    if (!aligned16(Qp) || !aligned16(A_g)) return HSS_ERR_MISALIGNED;
+    ScoreArgs a{};
+    a.Qp = Qp;
+    a.rows_per_seq = rows_per_seq;
+    a.A_g = A_g;
+    a.layer_offset_slots = static_cast<int64_t>(layer) * dims->max_blocks;
+    a.max_blocks = dims->max_blocks;
+    a.table = block_table;
+    a.seq_offsets = seq_offsets;
+    a.num_seqs = num_seqs;
+    a.total = total_blocks;
+    a.scores = scores;
+    a.num_q_heads = dims->num_q_heads;
+    a.num_kv_heads = dims->num_kv_heads;
+    a.r = dims->r;
+    a.block_size = dims->block_size;
+    a.dev_status = dev_status;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t nvec = static_cast<int64_t>(rows_per_seq) * (dims->num_q_heads / dims->num_kv_heads);
+    int chosen = path;
+    if (chosen == HSS_PATH_AUTO) {
+        chosen = (nvec <= 16 && score_decode_supported(a)) ? HSS_PATH_DECODE : HSS_PATH_TCGEN05;
+    }
+    if (chosen == HSS_PATH_DECODE) {
+        if (!score_decode_supported(a)) return HSS_ERR_UNSUPPORTED_SHAPE;
+        return launch_score_decode(a, s);
+    }
+    if (!score_tc_supported(a)) return HSS_ERR_UNSUPPORTED_SHAPE;
+    return launch_score_tc(a, s);
+}
+
+hss_status hss_rank_victims(const float* scores, const int32_t* seq_offsets, int32_t num_seqs,
+                            int64_t total_blocks, int32_t k, int32_t* victims, void* stream) {
+    if (num_seqs < 0 || total_blocks < 0 || total_blocks > 0x7FFFFFFF)
+        return HSS_ERR_INVALID_ARGUMENT;
+    if (k < 1 || k > HSS_MAX_VICTIMS) return HSS_ERR_INVALID_ARGUMENT;
+    if (num_seqs == 0) return HSS_OK;
+    if (seq_offsets == nullptr || victims == nullptr || (scores == nullptr && total_blocks > 0))
+        return HSS_ERR_NULL_POINTER;
+    return launch_rank_victims(scores, seq_offsets, num_seqs, total_blocks, k, victims,
+                               static_cast<cudaStream_t>(stream));
+}
+
+hss_status hss_read_device_error(int32_t* status, void* stream) {
+    if (status == nullptr) return HSS_ERR_NULL_POINTER;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (current_device_info() == nullptr) return HSS_ERR_CUDA;
+    int32_t v = 0;
+    const int32_t zero = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return HSS_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess) return HSS_ERR_CUDA;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero) != cudaSuccess) return HSS_ERR_CUDA;
+    *status = v;
+    return HSS_OK;
+}
+
+}  // extern "C"

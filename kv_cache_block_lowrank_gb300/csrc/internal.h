@@ -1,0 +1,77 @@
+// internal.h -- declarations shared by the library's translation units (host launchers and
+// the constants their kernels agree on).  Not part of the public C ABI (include/hss.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/hss.h"
+
+namespace hss {
+
+// A pipeline wait that has not completed after this much wall time is abandoned and
+// reported as HSS_ERR_DEVICE_TIMEOUT (no kernel here legitimately waits this long).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// Per-device facts the launchers need, read once per device.
+struct DeviceInfo {
+    int device = -1;
+    int num_sms = 0;
+    int max_smem_optin = 0;
+    int32_t* error_word = nullptr;  // library's own device error word (device address)
+};
+
+// Returns the info of the current device, initialising it on first use.  nullptr on failure.
+const DeviceInfo* current_device_info();
+
+// ------------------------------------------------------------------- projection (tcgen05)
+// Y rows = bf16(X rows . P).  X is [num_rows, head_dim] bf16.  Output row m goes to
+//   - Qp mode (block_ids == nullptr): out + m * r
+//   - A_g mode: row m = (i * block_size + t) * num_kv_heads + h goes to the A_g slot row
+//     ((layer * max_blocks + block_ids[i]) * num_kv_heads + h) * block_size + t.
+struct ProjectArgs {
+    const uint16_t* P;
+    const uint16_t* X;
+    int64_t num_rows;
+    int32_t head_dim;
+    int32_t r;
+    uint16_t* out;
+    // A_g mode only
+    const int32_t* block_ids;
+    int32_t num_kv_heads;
+    int32_t block_size;
+    int64_t max_blocks;
+    int32_t layer;
+    int32_t* dev_status;
+};
+hss_status launch_project(const ProjectArgs& a, cudaStream_t stream);
+bool project_shape_supported(int32_t head_dim, int32_t r);
+
+// ------------------------------------------------------------------- decode scorer
+struct ScoreArgs {
+    const uint16_t* Qp;
+    int32_t rows_per_seq;
+    const uint16_t* A_g;
+    int64_t layer_offset_slots;  // layer * max_blocks
+    int64_t max_blocks;
+    const int32_t* table;
+    const int32_t* seq_offsets;
+    int32_t num_seqs;
+    int64_t total;
+    float* scores;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t r;
+    int32_t block_size;
+    int32_t* dev_status;
+};
+hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream);
+bool score_decode_supported(const ScoreArgs& a);
+hss_status launch_score_tc(const ScoreArgs& a, cudaStream_t stream);
+bool score_tc_supported(const ScoreArgs& a);
+
+// ------------------------------------------------------------------- victims
+hss_status launch_rank_victims(const float* scores, const int32_t* seq_offsets, int32_t num_seqs,
+                               int64_t total, int32_t k, int32_t* victims, cudaStream_t stream);
+
+}  // namespace hss

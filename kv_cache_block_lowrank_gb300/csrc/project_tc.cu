@@ -1,0 +1,355 @@
+// project_tc.cu -- Q and K projection, Y = bf16(X . P), on the 5th-generation tensor cores.
+//
+// Page "metrale_storage/predictor.rs": Predictor::project_q (q_proj = q @ P, stored BF16) and
+// Predictor::project_kv_block (k_block [block_size, num_kv_heads, head_dim] projected into the
+// head-major A_g slot [num_kv_heads, block_size, r], stored BF16).  Both are the same skinny
+// GEMM -- rows of head_dim against P [head_dim, r] -- and differ only in where a result row
+// is stored, so one kernel serves both.
+//
+// Design (persistent, warp-specialised, one CTA per SM):
+//   warp 0      TMA producer: 128-row tiles of X, swizzled 128B, into a ring of smem stages
+//   warp 1      TMEM allocator and MMA issuer: tcgen05.mma M=128, N=r, K=16 steps, fp32
+//               accumulators double-buffered in TMEM (2 x r columns)
+//   warps 2..5  epilogue: tcgen05.ld a row per thread, round to bf16, store the row
+// P^T stays resident in shared memory (K-major, 128B swizzle) for the whole kernel.
+// The work is HBM-bound (head_dim * 2 bytes in, r * 2 bytes out per row); the tensor
+// cores only keep the arithmetic far below the memory time.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "ptx.cuh"
+
+namespace hss {
+namespace {
+
+constexpr int kBM = 128;            // rows per tile = UMMA M
+constexpr int kChunkElems = 64;     // bf16 elements per 128-byte swizzled row segment
+constexpr int kChunkBytes = kBM * 128;
+constexpr int kThreads = 192;
+constexpr int kMaxStages = 6;
+
+struct ProjLayout {
+    int kchunks = 0;       // head_dim / 64
+    int b_bytes = 0;       // P^T: kchunks * r * 128
+    int stage_bytes = 0;   // kchunks * 128 rows * 128 B
+    int stages = 0;
+    int bar_offset = 0;    // from the 1024-aligned base
+    int total_bytes = 0;   // dynamic smem to request (includes alignment slack)
+    int tmem_cols = 0;
+};
+
+__host__ __device__ inline int pow2_at_least(int x) {
+    int p = 32;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+__host__ __device__ inline ProjLayout make_layout(int head_dim, int r, int smem_budget) {
+    ProjLayout L;
+    L.kchunks = head_dim / kChunkElems;
+    L.b_bytes = L.kchunks * r * 128;
+    L.stage_bytes = L.kchunks * kChunkBytes;
+    const int fixed = 1024 /*align slack*/ + 256 /*barriers*/ + L.b_bytes;
+    int st = (smem_budget - fixed) / L.stage_bytes;
+    L.stages = st < kMaxStages ? st : kMaxStages;
+    L.bar_offset = L.b_bytes + L.stages * L.stage_bytes;
+    L.total_bytes = 1024 + L.bar_offset + 256;
+    L.tmem_cols = pow2_at_least(2 * r);
+    return L;
+}
+
+struct ProjParams {
+    const uint16_t* P;
+    int64_t num_rows;
+    int32_t head_dim;
+    int32_t r;
+    uint16_t* out;
+    const int32_t* block_ids;  // nullptr: Qp mode
+    int32_t num_kv_heads;
+    int32_t block_size;
+    int64_t max_blocks;
+    int64_t layer_slots;  // layer * max_blocks
+    int32_t* dev_status;
+    int32_t* lib_error;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    project_kernel(const __grid_constant__ CUtensorMap tmap_x, const ProjParams p, const int stages) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const ProjLayout L = make_layout(p.head_dim, p.r, 0x7FFFFFFF);  // sizes only
+    const int kchunks = L.kchunks;
+    const int stage_bytes = L.stage_bytes;
+    const int b_bytes = L.b_bytes;
+    uint8_t* sB = smem;
+    uint8_t* sA = smem + b_bytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sA + stages * stage_bytes);
+    uint64_t* empty = full + stages;
+    uint64_t* tfull = empty + stages;
+    uint64_t* tempty = tfull + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+    int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int r = p.r;
+    const int64_t num_tiles = (p.num_rows + kBM - 1) / kBM;
+
+    // P^T into shared memory, K-major with the 128-byte swizzle the MMA descriptor names:
+    // row j of chunk c holds P[64c .. 64c+63][j].
+    for (int e = threadIdx.x; e < p.head_dim * r; e += kThreads) {
+        const int d = e / r, j = e - (e / r) * r;
+        const uint16_t v = p.P[e];
+        const int c = d / kChunkElems, kk = d - c * kChunkElems;
+        *reinterpret_cast<uint16_t*>(sB + c * r * 128 + swizzled_offset(j, kk * 2, 128)) = v;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 4);
+        }
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    fence_proxy_async_smem();  // make the generic-proxy P^T writes visible to the tensor cores
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, L.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_x);
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t issued = 0;
+            for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u) || *(volatile int*)abort_flag) {
+                    raise_error(p.dev_status, p.lib_error, HSS_ERR_DEVICE_TIMEOUT);
+                    *(volatile int*)abort_flag = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(stage_bytes));
+                uint8_t* dst = sA + stage * stage_bytes;
+                for (int c = 0; c < kchunks; ++c) {
+                    tma_load_2d(dst + c * kChunkBytes, &tmap_x, &full[stage], c * kChunkElems,
+                                static_cast<int32_t>(tile * kBM));
+                }
+                ++issued;
+                if (++stage == stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            // Drain: every load this thread issued has landed before the CTA may exit.
+            const int64_t outstanding = issued < stages ? issued : stages;
+            for (int64_t q = 1; q <= outstanding; ++q) {
+                const int64_t n = issued - q;  // load number n used stage n % stages
+                const int st = static_cast<int>(n % stages);
+                const uint32_t ph = static_cast<uint32_t>((n / stages) & 1);
+                (void)mbar_wait(&full[st], ph);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>(r));
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t it = 0;
+            for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+                const int acc = static_cast<int>(it & 1);
+                const uint32_t acc_phase = static_cast<uint32_t>((it >> 1) & 1);
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u) || !mbar_wait(&full[stage], phase) ||
+                    *(volatile int*)abort_flag) {
+                    raise_error(p.dev_status, p.lib_error, HSS_ERR_DEVICE_TIMEOUT);
+                    *(volatile int*)abort_flag = 1;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * r);
+                const uint32_t a0 = smem_u32(sA + stage * stage_bytes);
+                const uint32_t b0 = smem_u32(sB);
+                for (int c = 0; c < kchunks; ++c) {
+                    for (int s = 0; s < kChunkElems / 16; ++s) {
+                        const uint64_t ad = smem_desc_kmajor(a0 + c * kChunkBytes + s * 32, 128);
+                        const uint64_t bd = smem_desc_kmajor(b0 + c * r * 128 + s * 32, 128);
+                        umma_bf16(d_tmem, ad, bd, idesc, (c | s) != 0 ? 1u : 0u);
+                    }
+                }
+                umma_commit(&empty[stage]);  // smem stage free once these MMAs have read it
+                umma_commit(&tfull[acc]);    // accumulator ready for the epilogue
+                if (++stage == stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    } else {
+        // Epilogue: warp w reads TMEM lanes 32 * (w % 4) .. + 31, one output row per thread.
+        const int quarter = warp & 3;
+        const int row_in_tile = quarter * 32 + lane;
+        const int rows_per_block = p.block_size * p.num_kv_heads;
+        int64_t it = 0;
+        for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+            const int acc = static_cast<int>(it & 1);
+            const uint32_t acc_phase = static_cast<uint32_t>((it >> 1) & 1);
+            const bool ok = mbar_wait(&tfull[acc], acc_phase);
+            if (__any_sync(0xffffffffu, !ok) || *(volatile int*)abort_flag) {
+                if (lane == 0) {
+                    raise_error(p.dev_status, p.lib_error, HSS_ERR_DEVICE_TIMEOUT);
+                    *(volatile int*)abort_flag = 1;
+                }
+                break;
+            }
+            tc_fence_after_sync();
+            const int64_t m = tile * kBM + row_in_tile;
+            uint16_t* dst = nullptr;
+            if (m < p.num_rows) {
+                if (p.block_ids == nullptr) {
+                    dst = p.out + m * r;
+                } else {
+                    const int64_t i = m / rows_per_block;
+                    const int rem = static_cast<int>(m - i * rows_per_block);
+                    const int t = rem / p.num_kv_heads;
+                    const int h = rem - t * p.num_kv_heads;
+                    const int64_t id = p.block_ids[i];
+                    if (id >= 0 && id < p.max_blocks) {
+                        dst = p.out + (((p.layer_slots + id) * p.num_kv_heads + h) * p.block_size +
+                                       t) * static_cast<int64_t>(r);
+                    } else if (rem == 0) {
+                        raise_error(p.dev_status, p.lib_error, HSS_ERR_OUT_OF_RANGE);
+                    }
+                }
+            }
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>(acc * r);
+            for (int c0 = 0; c0 < r; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld_32x32b_x16(taddr + c0, v);
+                tmem_ld_wait();
+                if (dst != nullptr) {
+                    uint4 o0, o1;
+                    o0.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
+                    o0.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
+                    o0.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
+                    o0.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
+                    o1.x = pack_bf16x2(__uint_as_float(v[8]), __uint_as_float(v[9]));
+                    o1.y = pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11]));
+                    o1.z = pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13]));
+                    o1.w = pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15]));
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+                    d4[0] = o0;
+                    d4[1] = o1;
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, L.tmem_cols);
+    }
+}
+
+// ------------------------------------------------------------------------------------- host
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess) {
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+    });
+    return g_encode;
+}
+
+// The smem attribute is set once per device (value = the largest request so far).
+int g_smem_set[64] = {0};
+std::mutex g_smem_mu;
+
+}  // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() { return encoder(); }
+
+bool project_shape_supported(int32_t head_dim, int32_t r) {
+    if (head_dim <= 0 || head_dim % kChunkElems != 0 || head_dim > 256) return false;
+    if (r < 16 || r > 256 || r % 16 != 0) return false;
+    const ProjLayout L = make_layout(head_dim, r, 232448);
+    return L.stages >= 2;
+}
+
+hss_status launch_project(const ProjectArgs& a, cudaStream_t stream) {
+    if (a.num_rows == 0) return HSS_OK;
+    const DeviceInfo* dev = current_device_info();
+    if (dev == nullptr) return HSS_ERR_CUDA;
+    if (!project_shape_supported(a.head_dim, a.r)) return HSS_ERR_UNSUPPORTED_SHAPE;
+    const ProjLayout L = make_layout(a.head_dim, a.r, dev->max_smem_optin);
+    if (L.stages < 2) return HSS_ERR_UNSUPPORTED_SHAPE;
+    auto enc = encoder();
+    if (enc == nullptr) return HSS_ERR_CUDA;
+
+    CUtensorMap tmap;
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(a.head_dim),
+                                static_cast<cuuint64_t>(a.num_rows)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(a.head_dim) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kChunkElems), static_cast<cuuint32_t>(kBM)};
+    const cuuint32_t estride[2] = {1, 1};
+    if (enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a.X), gdim, gstride,
+            box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+        return HSS_ERR_CUDA;
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_smem_mu);
+        const int d = dev->device & 63;
+        if (g_smem_set[d] < L.total_bytes) {
+            if (cudaFuncSetAttribute(project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     L.total_bytes) != cudaSuccess) {
+                return HSS_ERR_CUDA;
+            }
+            g_smem_set[d] = L.total_bytes;
+        }
+    }
+    ProjParams p;
+    p.P = a.P;
+    p.num_rows = a.num_rows;
+    p.head_dim = a.head_dim;
+    p.r = a.r;
+    p.out = a.out;
+    p.block_ids = a.block_ids;
+    p.num_kv_heads = a.num_kv_heads;
+    p.block_size = a.block_size;
+    p.max_blocks = a.max_blocks;
+    p.layer_slots = static_cast<int64_t>(a.layer) * a.max_blocks;
+    p.dev_status = a.dev_status;
+    p.lib_error = dev->error_word;
+    const int64_t num_tiles = (a.num_rows + kBM - 1) / kBM;
+    const int grid = static_cast<int>(std::min<int64_t>(num_tiles, dev->num_sms));
+    project_kernel<<<grid, kThreads, L.total_bytes, stream>>>(tmap, p, L.stages);
+    return cudaGetLastError() == cudaSuccess ? HSS_OK : HSS_ERR_CUDA;
+}
+
+}  // namespace hss

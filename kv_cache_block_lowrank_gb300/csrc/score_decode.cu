@@ -1,0 +1,320 @@
+// score_decode.cu -- block scores in the decode regime (few query vectors per kv head).
+//
+// Page "metrale_storage/predictor.rs", Predictor::score_blocks: each block's score is the max,
+// over query heads and the block's tokens, of the projected dot product Qp . A_g, where query
+// head h reads kv head h / g.  Here a block table and several query rows per sequence are
+// added; an identity table reproduces the page's contiguous slots.
+//
+// The regime is HBM-bound: each block's A_g slot (num_kv_heads * block_size * r bf16, 8 KiB
+// for the Llama-3-8B-like layer) is read exactly once, and only ~2 FMAs are done per byte.
+// Design:
+//   * one warp scores one block at a time; a warp owns a contiguous run of table entries;
+//   * the slot is read with 16-byte coalesced loads straight into registers -- all of a
+//     block's loads are issued before any arithmetic, so each warp keeps up to 8 KiB in flight;
+//   * the arithmetic runs on the warp-level tensor-core MMA (m16n8k16, bf16 in, fp32
+//     accumulate): tokens are the M side (16 per tile), the query vectors of one kv group
+//     (rows x g heads) the N side, r the K side.  Because the score only needs the dot product
+//     over r, the r-coordinates may be visited in any order as long as A and B use the same
+//     one; the order is chosen so that each lane's 16-byte load *is* its A fragment;
+//   * the query-vector fragments of the current sequence sit in a per-warp shared-memory
+//     cache in fragment order (one 8-byte load per MMA);
+//   * the max over tokens and query vectors is reduced in registers, then across the warp
+//     with shuffles; padded query-vector columns are masked to -inf.
+#include <algorithm>
+#include <cmath>
+
+#include "ptx.cuh"
+
+namespace hss {
+namespace {
+
+constexpr int kWarpsMax = 8;
+constexpr int kFragBudgetBytes = 48 * 1024;  // per CTA, all warps' fragment caches
+
+struct DecodeParams {
+    const uint16_t* Qp;
+    const uint16_t* A_g;
+    const int32_t* table;
+    const int32_t* seq_offsets;
+    float* scores;
+    int32_t* dev_status;
+    int32_t* lib_error;
+    int64_t layer_slots;
+    int64_t max_blocks;
+    int64_t total;
+    int64_t entries_per_warp;
+    int32_t num_seqs;
+    int32_t rows;
+    int32_t nq;
+    int32_t nkv;
+    int32_t r;
+    int32_t bs;
+    int32_t g;
+    int32_t nvec;  // rows * g query vectors per kv head
+};
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Physical r-offset of the 4 elements that lane quad t holds for k-step ks
+// (KSTEPS even: each 16-byte load covers two k-steps; KSTEPS == 1: 8-byte loads).
+template <int KSTEPS>
+__device__ __forceinline__ int frag_r_offset(int ks, int t) {
+    if constexpr (KSTEPS == 1) {
+        return 4 * t;
+    } else {
+        return 32 * (ks >> 1) + 8 * t + 4 * (ks & 1);
+    }
+}
+
+template <int KSTEPS, int NT>
+__global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const DecodeParams p) {
+    extern __shared__ uint2 frag_cache_all[];
+    constexpr int kLoadsPerRow = KSTEPS == 1 ? 1 : KSTEPS / 2;  // 16-byte (or 8-byte) loads
+    constexpr int kRegsPerTile = KSTEPS == 1 ? 4 : 4 * KSTEPS;  // both row halves
+    constexpr int kTilesPerBatch = 64 / kRegsPerTile;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int gq = lane >> 2;  // MMA group id: token row (A), query vector column (B)
+    const int tq = lane & 3;   // thread in group
+    const int frag_per_warp = p.nkv * KSTEPS * NT * 32;
+    uint2* cache = frag_cache_all + warp * frag_per_warp;
+
+    const int64_t wid = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + warp;
+    const int64_t i_begin = wid * p.entries_per_warp;
+    if (i_begin >= p.total) return;
+    const int64_t i_end = min(p.total, i_begin + p.entries_per_warp);
+
+    // Sequence of the first entry: the last s with seq_offsets[s] <= i_begin.
+    int lo = 0, hi = p.num_seqs;  // invariant: seq_offsets[lo] <= i_begin < seq_offsets[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (static_cast<int64_t>(__ldg(&p.seq_offsets[mid])) <= i_begin) lo = mid; else hi = mid;
+    }
+    int s = lo;
+    int64_t seq_end = __ldg(&p.seq_offsets[s + 1]);
+    int cached_seq = -1;
+
+    const int tiles_per_head = p.bs >> 4;
+    const int num_tiles = p.nkv * tiles_per_head;
+    const int64_t slot_elems = static_cast<int64_t>(p.nkv) * p.bs * p.r;
+    const int64_t tile_elems = 16 * static_cast<int64_t>(p.r);
+
+    // Column validity of this lane's accumulator entries (query vector index < nvec).
+    bool col_ok[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        col_ok[nt][0] = nt * 8 + 2 * tq < p.nvec;
+        col_ok[nt][1] = nt * 8 + 2 * tq + 1 < p.nvec;
+    }
+
+    for (int64_t i0 = i_begin; i0 < i_end; i0 += 32) {
+        const int64_t left = i_end - i0;
+        const int n_here = left < 32 ? static_cast<int>(left) : 32;
+        const int32_t my_id = lane < n_here ? __ldg(&p.table[i0 + lane]) : 0;
+        for (int e = 0; e < n_here; ++e) {
+            const int64_t i = i0 + e;
+            while (i >= seq_end && s + 1 < p.num_seqs) {
+                ++s;
+                seq_end = __ldg(&p.seq_offsets[s + 1]);
+            }
+            if (s != cached_seq) {
+                // Query-vector fragments of sequence s, in MMA B-fragment order.
+                __syncwarp();
+                for (int c = 0; c < p.nkv; ++c) {
+#pragma unroll
+                    for (int ks = 0; ks < KSTEPS; ++ks) {
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const int v = nt * 8 + gq;
+                            uint2 f = make_uint2(0u, 0u);
+                            if (v < p.nvec) {
+                                const int row = v / p.g;
+                                const int h = c * p.g + (v - row * p.g);
+                                const uint16_t* q =
+                                    p.Qp + ((static_cast<int64_t>(s) * p.rows + row) * p.nq + h) *
+                                               p.r;
+                                f = *reinterpret_cast<const uint2*>(q + frag_r_offset<KSTEPS>(ks, tq));
+                            }
+                            cache[((c * KSTEPS + ks) * NT + nt) * 32 + lane] = f;
+                        }
+                    }
+                }
+                __syncwarp();
+                cached_seq = s;
+            }
+            const int32_t id = __shfl_sync(0xffffffffu, my_id, e);
+            if (id < 0 || id >= p.max_blocks) {
+                if (lane == 0) {
+                    p.scores[i] = INFINITY;
+                    raise_error(p.dev_status, p.lib_error, HSS_ERR_OUT_OF_RANGE);
+                }
+                continue;
+            }
+            const uint16_t* slot = p.A_g + (p.layer_slots + id) * slot_elems;
+            float best = -INFINITY;
+            for (int tb = 0; tb < num_tiles; tb += kTilesPerBatch) {
+                uint32_t data[kTilesPerBatch][kRegsPerTile];
+                // Issue every load of the batch first.
+#pragma unroll
+                for (int u = 0; u < kTilesPerBatch; ++u) {
+                    const int tile = tb + u;
+                    if (tile < num_tiles) {
+                        const uint16_t* base = slot + tile * tile_elems;
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            const uint16_t* rowp = base + (gq + 8 * half) * p.r;
+#pragma unroll
+                            for (int l = 0; l < kLoadsPerRow; ++l) {
+                                if constexpr (KSTEPS == 1) {
+                                    const uint2 v = __ldcs(reinterpret_cast<const uint2*>(rowp + 4 * tq));
+                                    data[u][half * 2 + 0] = v.x;
+                                    data[u][half * 2 + 1] = v.y;
+                                } else {
+                                    const uint4 v = __ldcs(
+                                        reinterpret_cast<const uint4*>(rowp + 32 * l + 8 * tq));
+                                    data[u][(half * kLoadsPerRow + l) * 4 + 0] = v.x;
+                                    data[u][(half * kLoadsPerRow + l) * 4 + 1] = v.y;
+                                    data[u][(half * kLoadsPerRow + l) * 4 + 2] = v.z;
+                                    data[u][(half * kLoadsPerRow + l) * 4 + 3] = v.w;
+                                }
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kTilesPerBatch; ++u) {
+                    const int tile = tb + u;
+                    if (tile < num_tiles) {
+                        const int c = tile / tiles_per_head;
+                        float acc[NT][4];
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+                        for (int ks = 0; ks < KSTEPS; ++ks) {
+                            uint32_t a0, a1, a2, a3;
+                            if constexpr (KSTEPS == 1) {
+                                a0 = data[u][0];  // token row gq,     r 4t..4t+1
+                                a2 = data[u][1];  // token row gq,     r 4t+2..4t+3
+                                a1 = data[u][2];  // token row gq + 8
+                                a3 = data[u][3];
+                            } else {
+                                const int l = ks >> 1, w = ks & 1;
+                                a0 = data[u][(0 * kLoadsPerRow + l) * 4 + 2 * w + 0];
+                                a2 = data[u][(0 * kLoadsPerRow + l) * 4 + 2 * w + 1];
+                                a1 = data[u][(1 * kLoadsPerRow + l) * 4 + 2 * w + 0];
+                                a3 = data[u][(1 * kLoadsPerRow + l) * 4 + 2 * w + 1];
+                            }
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                const uint2 b = cache[((c * KSTEPS + ks) * NT + nt) * 32 + lane];
+                                mma_bf16_16816(acc[nt], a0, a1, a2, a3, b.x, b.y);
+                            }
+                        }
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            if (col_ok[nt][0]) best = fmaxf(best, fmaxf(acc[nt][0], acc[nt][2]));
+                            if (col_ok[nt][1]) best = fmaxf(best, fmaxf(acc[nt][1], acc[nt][3]));
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, off));
+            if (lane == 0) p.scores[i] = best;
+        }
+    }
+}
+
+template <int KSTEPS, int NT>
+hss_status launch_t(const DecodeParams& p, int warps_per_cta, int smem, int grid,
+                    cudaStream_t stream) {
+    auto k = score_decode_kernel<KSTEPS, NT>;
+    if (smem > 48 * 1024) {
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
+            return HSS_ERR_CUDA;
+    }
+    k<<<grid, warps_per_cta * 32, smem, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? HSS_OK : HSS_ERR_CUDA;
+}
+
+int frag_bytes_per_warp(const ScoreArgs& a) {
+    const int ksteps = a.r / 16;
+    const int nvec = a.rows_per_seq * (a.num_q_heads / a.num_kv_heads);
+    const int nt = (nvec + 7) / 8;
+    return a.num_kv_heads * ksteps * nt * 32 * 8;
+}
+
+}  // namespace
+
+bool score_decode_supported(const ScoreArgs& a) {
+    if (a.block_size % 16 != 0 || a.r % 16 != 0) return false;
+    const int ksteps = a.r / 16;
+    if (ksteps != 1 && ksteps != 2 && ksteps != 4 && ksteps != 8) return false;
+    const int64_t nvec = static_cast<int64_t>(a.rows_per_seq) * (a.num_q_heads / a.num_kv_heads);
+    if (nvec < 1 || nvec > 16) return false;
+    return frag_bytes_per_warp(a) <= kFragBudgetBytes;
+}
+
+hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream) {
+    if (a.total == 0) return HSS_OK;
+    const DeviceInfo* dev = current_device_info();
+    if (dev == nullptr) return HSS_ERR_CUDA;
+    if (!score_decode_supported(a)) return HSS_ERR_UNSUPPORTED_SHAPE;
+    DecodeParams p;
+    p.Qp = a.Qp;
+    p.A_g = a.A_g;
+    p.table = a.table;
+    p.seq_offsets = a.seq_offsets;
+    p.scores = a.scores;
+    p.dev_status = a.dev_status;
+    p.lib_error = dev->error_word;
+    p.layer_slots = a.layer_offset_slots;
+    p.max_blocks = a.max_blocks;
+    p.total = a.total;
+    p.num_seqs = a.num_seqs;
+    p.rows = a.rows_per_seq;
+    p.nq = a.num_q_heads;
+    p.nkv = a.num_kv_heads;
+    p.r = a.r;
+    p.bs = a.block_size;
+    p.g = a.num_q_heads / a.num_kv_heads;
+    p.nvec = a.rows_per_seq * p.g;
+
+    const int fb = frag_bytes_per_warp(a);
+    const int warps_per_cta = std::max(1, std::min(kWarpsMax, kFragBudgetBytes / fb));
+    const int smem = warps_per_cta * fb;
+    // Enough warps for two CTAs per SM; each warp takes a contiguous run of entries.
+    const int64_t target_warps = static_cast<int64_t>(dev->num_sms) * 2 * warps_per_cta;
+    p.entries_per_warp = std::max<int64_t>(1, (a.total + target_warps - 1) / target_warps);
+    const int64_t warps = (a.total + p.entries_per_warp - 1) / p.entries_per_warp;
+    const int grid = static_cast<int>((warps + warps_per_cta - 1) / warps_per_cta);
+
+    const int ksteps = a.r / 16;
+    const int nt = (p.nvec + 7) / 8;
+#define HSS_DECODE_CASE(KS, NT_)                                                        \
+    if (ksteps == KS && nt == NT_) return launch_t<KS, NT_>(p, warps_per_cta, smem, grid, stream);
+    HSS_DECODE_CASE(1, 1)
+    HSS_DECODE_CASE(1, 2)
+    HSS_DECODE_CASE(2, 1)
+    HSS_DECODE_CASE(2, 2)
+    HSS_DECODE_CASE(4, 1)
+    HSS_DECODE_CASE(4, 2)
+    HSS_DECODE_CASE(8, 1)
+    HSS_DECODE_CASE(8, 2)
+#undef HSS_DECODE_CASE
+    return HSS_ERR_UNSUPPORTED_SHAPE;
+}
+
+}  // namespace hss
