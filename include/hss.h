@@ -42,8 +42,8 @@ extern "C" {
 /* The seven predictor dimensions (PredictorDims on the predictor page).
  * num_q_heads must be a multiple of num_kv_heads (PredictorDims::validate);
  * query head h reads kv head h / (num_q_heads / num_kv_heads).
- * Shapes the kernels support: head_dim in {16, 32, 64, 128, 192, 256};
- * r a multiple of 16 in [16, 256]; block_size a multiple of 16 in [16, 256];
+ * Shapes the kernels support: head_dim in {64, 128, 192, 256}; r in {16, 32, 64, 128};
+ * block_size a multiple of 16 in [16, 256] (the tensor-core scorer: 16 or 32);
  * num_kv_heads <= 64; max_blocks <= 2^31 - 1. */
 typedef struct hss_dims {
     int32_t num_layers;

@@ -50,7 +50,7 @@ static hss_status check_dims(const hss_dims* d) {
     if (d->num_q_heads % d->num_kv_heads != 0) return HSS_ERR_INVALID_DIMS;
     if (d->max_blocks > 0x7FFFFFFF) return HSS_ERR_UNSUPPORTED_SHAPE;
     if (d->num_kv_heads > 64) return HSS_ERR_UNSUPPORTED_SHAPE;
-    if (d->r % 16 != 0 || d->r > 256) return HSS_ERR_UNSUPPORTED_SHAPE;
+    if (d->r != 16 && d->r != 32 && d->r != 64 && d->r != 128) return HSS_ERR_UNSUPPORTED_SHAPE;
     if (d->block_size % 16 != 0 || d->block_size > 256) return HSS_ERR_UNSUPPORTED_SHAPE;
     if (d->head_dim % 64 != 0 || d->head_dim > 256) return HSS_ERR_UNSUPPORTED_SHAPE;
     return HSS_OK;

@@ -1,17 +1,510 @@
-// score_tc.cu -- block scores for prefill chunks on the tcgen05 tensor cores (not built yet).
+// score_tc.cu -- block scores for prefill chunks on the 5th-generation tensor cores.
+//
+// Page "metrale_storage/predictor.rs", Predictor::score_blocks: a block's score is the max,
+// over query heads and tokens, of the projected dot product Qp . A_g (query head h reads kv
+// head h / g).  With a prefill chunk of R query rows there are R * g query vectors per kv
+// head, and Qp . A_g^T becomes a real dense contraction (R * g x tokens x r per kv head), so
+// it runs on tcgen05.mma with TMEM accumulators.
+//
+// Orientation: tokens are the M side (128-token tiles = 128 / block_size blocks of one kv
+// head, gathered through the block table with one TMA box per block), query vectors the N
+// side, r the K side.  Then every TMEM lane (= thread in the epilogue) holds one token's
+// dot products with 256 query vectors: the max over query vectors is a per-thread register
+// reduction, and the max over a block's tokens is a 16-lane shuffle reduction.
+//
+// Work units: (sequence s, kv head c, slice of up to 1024 query vectors, 128-token tile).
+// A slice of Qp stays resident in shared memory (B operand, K-major, swizzled) while the
+// CTA streams token tiles; each CTA takes a contiguous run of units, so it reloads Qp only
+// when its run crosses into the next (s, c, slice).  Roles (persistent, 1 CTA per SM):
+//   warp 0      TMA producer (Qp slices; per-block A_g boxes into a ring of stages)
+//   warp 1      TMEM allocator (512 columns) and MMA issuer, M=128, N=256, K=16 steps
+//   warps 2..5  epilogue: tcgen05.ld, running max per token, block max, float atomic max
+// Scores are first set to -inf (separate tiny kernel); every unit atomically maxes its
+// partial block maximum into the block's score.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
 #include "ptx.cuh"
 
 namespace hss {
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kTileTokens = 128;     // UMMA M
+constexpr int kNChunk = 256;         // UMMA N per accumulator buffer
+constexpr int kMaxSliceVecs = 1024;  // query vectors resident per slice
+constexpr int kMaxSeqs = 1024;       // prefix table of units per sequence lives in smem
+constexpr int kBudgetB = 128 * 1024;
+
+struct TcLayout {
+    int row_bytes;      // bytes of one swizzled row segment: min(r, 64) * 2
+    int kchunks;        // r / (row_bytes / 2)
+    int slice;          // query vectors per slice (multiple of 256)
+    int b_bytes;        // slice * r * 2
+    int a_stage_bytes;  // 128 * r * 2
+    int stages;
+    int total_bytes;
+};
+
+TcLayout make_tc_layout(int r, int smem_budget) {
+    TcLayout L;
+    L.row_bytes = (r >= 64 ? 64 : r) * 2;
+    L.kchunks = r * 2 / L.row_bytes;
+    int slice = kBudgetB / (r * 2);
+    slice = slice / kNChunk * kNChunk;
+    L.slice = std::min(kMaxSliceVecs, std::max(kNChunk, slice));
+    L.b_bytes = L.slice * r * 2;
+    L.a_stage_bytes = kTileTokens * r * 2;
+    const int fixed = 1024 + 512 + (kMaxSeqs + 1) * 8 + L.b_bytes;
+    L.stages = std::min(4, (smem_budget - fixed) / L.a_stage_bytes);
+    L.total_bytes = fixed + L.stages * L.a_stage_bytes;
+    return L;
+}
+
+struct TcParams {
+    const int32_t* table;
+    const int32_t* seq_offsets;
+    float* scores;
+    int32_t* dev_status;
+    int32_t* lib_error;
+    int64_t layer_slots;  // layer * max_blocks
+    int64_t max_blocks;
+    int64_t total_units;
+    int64_t units_per_cta;
+    int32_t num_seqs;
+    int32_t nkv;
+    int32_t g;
+    int32_t bs;
+    int32_t r;
+    int32_t rows;  // query rows per sequence
+    int32_t nvec;  // rows * g query vectors per (sequence, kv head)
+    int32_t nslices;
+    int32_t slice;
+    int32_t bpt;  // blocks per 128-token tile
+    int32_t row_bytes;
+    int32_t kchunks;
+    int32_t b_bytes;
+    int32_t a_stage_bytes;
+    int32_t stages;
+};
+
+struct Unit {
+    int s, c, q;
+    int64_t t;       // tile within the sequence
+    int64_t first;   // table index of the sequence's first block
+    int64_t end;     // one past its last
+    int64_t pair;    // (s, c, q) identity
+};
+
+// Unit u -> (sequence, kv head, slice, tile), with units_before[s] = units of sequences < s.
+__device__ __forceinline__ Unit decode_unit(int64_t u, const TcParams& p,
+                                            const int64_t* units_before) {
+    int lo = 0, hi = p.num_seqs;  // last s with units_before[s] <= u
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (units_before[mid] <= u) lo = mid; else hi = mid;
+    }
+    Unit x;
+    x.s = lo;
+    x.first = p.seq_offsets[lo];
+    x.end = p.seq_offsets[lo + 1];
+    const int64_t tiles = (x.end - x.first + p.bpt - 1) / p.bpt;
+    const int64_t local = u - units_before[lo];
+    const int64_t pl = local / tiles;
+    x.t = local - pl * tiles;
+    x.c = static_cast<int>(pl / p.nslices);
+    x.q = static_cast<int>(pl - static_cast<int64_t>(x.c) * p.nslices);
+    x.pair = units_before[lo] + pl * tiles;  // unique per (s, c, q)
+    return x;
+}
+
+__device__ __forceinline__ void atomic_max_f32(float* addr, float v) {
+    v = v + 0.0f;  // -0 -> +0, so the integer orderings below agree with the float order
+    if (v >= 0.0f) {
+        atomicMax(reinterpret_cast<int*>(addr), __float_as_int(v));
+    } else {
+        atomicMin(reinterpret_cast<unsigned int*>(addr), __float_as_uint(v));
+    }
+}
+
+__global__ void fill_neg_inf(float* __restrict__ x, int64_t n) {
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        x[i] = -INFINITY;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    score_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                    const __grid_constant__ CUtensorMap tmap_q, const TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* sB = smem;
+    uint8_t* sA = sB + p.b_bytes;
+    uint64_t* a_full = reinterpret_cast<uint64_t*>(sA + p.stages * p.a_stage_bytes);
+    uint64_t* a_empty = a_full + p.stages;
+    uint64_t* b_full = a_empty + p.stages;
+    uint64_t* b_empty = b_full + 1;
+    uint64_t* t_full = b_empty + 1;
+    uint64_t* t_empty = t_full + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(t_empty + 2);
+    int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+    int64_t* units_before = reinterpret_cast<int64_t*>(smem + p.b_bytes +
+                                                       p.stages * p.a_stage_bytes + 512);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    constexpr uint32_t kTmemCols = 512;
+
+    // Units before each sequence: nkv * nslices * tiles(s) per sequence.
+    if (threadIdx.x == 0) {
+        int64_t acc = 0;
+        for (int s = 0; s < p.num_seqs; ++s) {
+            units_before[s] = acc;
+            const int64_t n = static_cast<int64_t>(p.seq_offsets[s + 1]) - p.seq_offsets[s];
+            acc += static_cast<int64_t>(p.nkv) * p.nslices * ((n + p.bpt - 1) / p.bpt);
+        }
+        units_before[p.num_seqs] = acc;
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&a_full[s], 1);
+            mbar_init(&a_empty[s], 1);
+        }
+        mbar_init(b_full, 1);
+        mbar_init(b_empty, 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&t_full[a], 1);
+            mbar_init(&t_empty[a], 4);
+        }
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    // The host sized the grid from an upper bound; the exact count is units_before[num_seqs].
+    const int64_t u_begin = static_cast<int64_t>(blockIdx.x) * p.units_per_cta;
+    const int64_t u_end = min(units_before[p.num_seqs], u_begin + p.units_per_cta);
+    const int nchunks = p.slice / kNChunk;
+    const int elems_per_row = p.row_bytes / 2;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_a);
+            tma_prefetch_desc(&tmap_q);
+            int stage = 0;
+            uint32_t phase = 0, b_empty_phase = 0, b_loads = 0;
+            int64_t prev_pair = -1, issued = 0;
+            bool ok = true;
+            for (int64_t u = u_begin; u < u_end && ok; ++u) {
+                const Unit x = decode_unit(u, p, units_before);
+                if (x.pair != prev_pair) {
+                    if (prev_pair >= 0) {
+                        ok = mbar_wait(b_empty, b_empty_phase);
+                        b_empty_phase ^= 1u;
+                        if (!ok) break;
+                    }
+                    mbar_arrive_expect_tx(b_full, static_cast<uint32_t>(p.b_bytes));
+                    for (int kc = 0; kc < p.kchunks; ++kc) {
+                        for (int j = 0; j < nchunks; ++j) {
+                            const int64_t z = static_cast<int64_t>(x.s) * p.rows +
+                                              (static_cast<int64_t>(x.q) * p.slice +
+                                               j * kNChunk) / p.g;
+                            tma_load_3d(sB + kc * (p.slice * p.row_bytes) +
+                                            j * (kNChunk * p.row_bytes),
+                                        &tmap_q, b_full, kc * elems_per_row, x.c * p.g,
+                                        static_cast<int32_t>(z));
+                        }
+                    }
+                    ++b_loads;
+                    prev_pair = x.pair;
+                }
+                if (!mbar_wait(&a_empty[stage], phase ^ 1u) || *(volatile int*)abort_flag) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&a_full[stage], static_cast<uint32_t>(p.a_stage_bytes));
+                uint8_t* dst = sA + stage * p.a_stage_bytes;
+                for (int blk = 0; blk < p.bpt; ++blk) {
+                    const int64_t e = x.first + x.t * p.bpt + blk;
+                    int64_t id = e < x.end ? static_cast<int64_t>(p.table[e]) : -1;
+                    if (id < 0 || id >= p.max_blocks) id = 0;  // a dummy box; never scored
+                    const int64_t row = ((p.layer_slots + id) * p.nkv + x.c) * p.bs;
+                    for (int kc = 0; kc < p.kchunks; ++kc) {
+                        tma_load_2d(dst + kc * (kTileTokens * p.row_bytes) +
+                                        blk * p.bs * p.row_bytes,
+                                    &tmap_a, &a_full[stage], kc * elems_per_row,
+                                    static_cast<int32_t>(row));
+                    }
+                }
+                ++issued;
+                if (++stage == p.stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) {
+                raise_error(p.dev_status, p.lib_error, HSS_ERR_DEVICE_TIMEOUT);
+                *(volatile int*)abort_flag = 1;
+            }
+            // Drain: every copy this thread started has landed before the CTA may exit.
+            const int64_t outstanding = issued < p.stages ? issued : p.stages;
+            for (int64_t k = 1; k <= outstanding; ++k) {
+                const int64_t n = issued - k;
+                (void)mbar_wait(&a_full[n % p.stages], static_cast<uint32_t>((n / p.stages) & 1));
+            }
+            if (b_loads > 0) (void)mbar_wait(b_full, (b_loads - 1) & 1u);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kTileTokens, kNChunk);
+            int stage = 0;
+            uint32_t phase = 0, b_full_phase = 0;
+            int64_t prev_pair = -1, it = 0;
+            bool ok = true;
+            for (int64_t u = u_begin; u < u_end && ok; ++u) {
+                const Unit x = decode_unit(u, p, units_before);
+                if (x.pair != prev_pair) {
+                    if (prev_pair >= 0) umma_commit(b_empty);  // old slice free once MMAs finish
+                    ok = mbar_wait(b_full, b_full_phase);
+                    b_full_phase ^= 1u;
+                    prev_pair = x.pair;
+                    if (!ok) break;
+                }
+                if (!mbar_wait(&a_full[stage], phase) || *(volatile int*)abort_flag) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t a0 = smem_u32(sA + stage * p.a_stage_bytes);
+                const uint32_t b0 = smem_u32(sB);
+                for (int nc = 0; nc < nchunks && ok; ++nc, ++it) {
+                    const int acc = static_cast<int>(it & 1);
+                    if (!mbar_wait(&t_empty[acc], static_cast<uint32_t>(((it >> 1) & 1) ^ 1))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kNChunk);
+                    for (int kc = 0; kc < p.kchunks; ++kc) {
+                        for (int ks = 0; ks < elems_per_row / 16; ++ks) {
+                            const uint64_t ad = smem_desc_kmajor(
+                                a0 + kc * (kTileTokens * p.row_bytes) + ks * 32, p.row_bytes);
+                            const uint64_t bd = smem_desc_kmajor(
+                                b0 + kc * (p.slice * p.row_bytes) + nc * (kNChunk * p.row_bytes) +
+                                    ks * 32,
+                                p.row_bytes);
+                            umma_bf16(d_tmem, ad, bd, idesc, (kc | ks) != 0 ? 1u : 0u);
+                        }
+                    }
+                    umma_commit(&t_full[acc]);
+                }
+                umma_commit(&a_empty[stage]);
+                if (++stage == p.stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) {
+                raise_error(p.dev_status, p.lib_error, HSS_ERR_DEVICE_TIMEOUT);
+                *(volatile int*)abort_flag = 1;
+            }
+        }
+    } else {
+        // Epilogue: warp w owns TMEM lanes 32 * (w % 4) .. + 31 = token rows of the tile.
+        const int quarter = warp & 3;
+        const int token = quarter * 32 + lane;
+        int64_t it = 0;
+        bool ok = true;
+        for (int64_t u = u_begin; u < u_end && ok; ++u) {
+            const Unit x = decode_unit(u, p, units_before);
+            float run = -INFINITY;
+            for (int nc = 0; nc < nchunks; ++nc, ++it) {
+                const int acc = static_cast<int>(it & 1);
+                const bool got = mbar_wait(&t_full[acc], static_cast<uint32_t>((it >> 1) & 1));
+                if (__any_sync(0xffffffffu, !got) || *(volatile int*)abort_flag) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const int v0 = x.q * p.slice + nc * kNChunk;  // first query vector of the chunk
+                const int valid = min(kNChunk, p.nvec - v0);
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                       static_cast<uint32_t>(acc * kNChunk);
+                for (int c0 = 0; c0 < kNChunk; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(taddr + c0, v);
+                    tmem_ld_wait();
+                    if (c0 + 32 <= valid) {
+                        float m0 = __uint_as_float(v[0]), m1 = __uint_as_float(v[1]);
+#pragma unroll
+                        for (int j = 2; j < 32; j += 2) {
+                            m0 = fmaxf(m0, __uint_as_float(v[j]));
+                            m1 = fmaxf(m1, __uint_as_float(v[j + 1]));
+                        }
+                        run = fmaxf(run, fmaxf(m0, m1));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (c0 + j < valid) run = fmaxf(run, __uint_as_float(v[j]));
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&t_empty[acc]);
+            }
+            if (!ok) break;
+            // Max over the block's tokens: block_size consecutive lanes.
+            for (int off = p.bs >> 1; off > 0; off >>= 1)
+                run = fmaxf(run, __shfl_xor_sync(0xffffffffu, run, off));
+            if ((lane & (p.bs - 1)) == 0) {
+                const int blk = token / p.bs;
+                const int64_t e = x.first + x.t * p.bpt + blk;
+                if (e < x.end) {
+                    const int64_t id = p.table[e];
+                    if (id >= 0 && id < p.max_blocks) {
+                        atomic_max_f32(p.scores + e, run);
+                    } else {
+                        atomic_max_f32(p.scores + e, INFINITY);
+                        if (x.c == 0 && x.q == 0)
+                            raise_error(p.dev_status, p.lib_error, HSS_ERR_OUT_OF_RANGE);
+                    }
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            raise_error(p.dev_status, p.lib_error, HSS_ERR_DEVICE_TIMEOUT);
+            *(volatile int*)abort_flag = 1;
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+int g_smem_set[64] = {0};
+std::mutex g_smem_mu;
+
+}  // namespace
+
 bool score_tc_supported(const ScoreArgs& a) {
-    (void)a;
-    return false;
+    if (a.num_seqs < 1 || a.num_seqs > kMaxSeqs) return false;
+    if (a.block_size != 16 && a.block_size != 32) return false;
+    if (a.r % 16 != 0 || a.r < 16 || a.r > 256) return false;
+    const int g = a.num_q_heads / a.num_kv_heads;
+    if (g < 1 || g > kNChunk || kNChunk % g != 0) return false;
+    if (a.r > 64 && a.r % 64 != 0) return false;
+    const TcLayout L = make_tc_layout(a.r, 232448);
+    return L.stages >= 2;
 }
 
 hss_status launch_score_tc(const ScoreArgs& a, cudaStream_t stream) {
-    (void)a;
-    (void)stream;
-    return HSS_ERR_UNSUPPORTED_SHAPE;
+    if (a.total == 0) return HSS_OK;
+    const DeviceInfo* dev = current_device_info();
+    if (dev == nullptr) return HSS_ERR_CUDA;
+    if (!score_tc_supported(a)) return HSS_ERR_UNSUPPORTED_SHAPE;
+    const TcLayout L = make_tc_layout(a.r, dev->max_smem_optin);
+    if (L.stages < 2) return HSS_ERR_UNSUPPORTED_SHAPE;
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return HSS_ERR_CUDA;
+    const int g = a.num_q_heads / a.num_kv_heads;
+    const int elems = L.row_bytes / 2;
+    const CUtensorMapSwizzle sw = L.row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : L.row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                      : CU_TENSOR_MAP_SWIZZLE_32B;
+    // A_g as rows of r: row ((layer * max_blocks + id) * nkv + c) * bs + t.  The map spans
+    // every layer up to the scored one, so rows of the scored layer are in range.
+    CUtensorMap tmap_a, tmap_q;
+    {
+        const uint64_t rows = static_cast<uint64_t>(a.layer_offset_slots + a.max_blocks) *
+                              a.num_kv_heads * a.block_size;
+        const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(a.r), rows};
+        const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(a.r) * 2};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(elems),
+                                   static_cast<cuuint32_t>(a.block_size)};
+        const cuuint32_t es[2] = {1, 1};
+        if (enc(&tmap_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a.A_g), gdim,
+                gstride, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return HSS_ERR_CUDA;
+    }
+    {
+        // Qp as [num_seqs * rows][num_q_heads][r]; a box is 256 query vectors of one kv
+        // head: (256 / g) rows x g heads x one swizzled row segment.
+        const cuuint64_t gdim[3] = {static_cast<cuuint64_t>(a.r),
+                                    static_cast<cuuint64_t>(a.num_q_heads),
+                                    static_cast<cuuint64_t>(a.num_seqs) * a.rows_per_seq};
+        const cuuint64_t gstride[2] = {static_cast<cuuint64_t>(a.r) * 2,
+                                       static_cast<cuuint64_t>(a.num_q_heads) * a.r * 2};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(elems), static_cast<cuuint32_t>(g),
+                                   static_cast<cuuint32_t>(kNChunk / g)};
+        const cuuint32_t es[3] = {1, 1, 1};
+        if (enc(&tmap_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(a.Qp), gdim,
+                gstride, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return HSS_ERR_CUDA;
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_smem_mu);
+        const int d = dev->device & 63;
+        if (g_smem_set[d] < L.total_bytes) {
+            if (cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     L.total_bytes) != cudaSuccess)
+                return HSS_ERR_CUDA;
+            g_smem_set[d] = L.total_bytes;
+        }
+    }
+    TcParams p;
+    p.table = a.table;
+    p.seq_offsets = a.seq_offsets;
+    p.scores = a.scores;
+    p.dev_status = a.dev_status;
+    p.lib_error = dev->error_word;
+    p.layer_slots = a.layer_offset_slots;
+    p.max_blocks = a.max_blocks;
+    p.num_seqs = a.num_seqs;
+    p.nkv = a.num_kv_heads;
+    p.g = g;
+    p.bs = a.block_size;
+    p.r = a.r;
+    p.rows = a.rows_per_seq;
+    p.nvec = a.rows_per_seq * g;
+    p.slice = std::min(L.slice, (p.nvec + kNChunk - 1) / kNChunk * kNChunk);
+    p.b_bytes = p.slice * a.r * 2;
+    p.nslices = (p.nvec + p.slice - 1) / p.slice;
+    p.bpt = kTileTokens / a.block_size;
+    p.row_bytes = L.row_bytes;
+    p.kchunks = L.kchunks;
+    p.a_stage_bytes = L.a_stage_bytes;
+    p.stages = L.stages;
+    // Unit count: exact for one sequence; otherwise an upper bound (the offsets live on the
+    // device), since every sequence contributes ceil(n_s / bpt) <= n_s / bpt + 1 tiles.
+    const int64_t max_tiles = a.num_seqs == 1 ? (a.total + p.bpt - 1) / p.bpt
+                                              : a.total / p.bpt + a.num_seqs;
+    p.total_units = static_cast<int64_t>(p.nkv) * p.nslices * max_tiles;
+    const int grid = static_cast<int>(std::min<int64_t>(dev->num_sms, p.total_units));
+    p.units_per_cta = (p.total_units + grid - 1) / grid;
+
+    const int fill_grid = static_cast<int>(std::min<int64_t>((a.total + 255) / 256, 1024));
+    fill_neg_inf<<<fill_grid, 256, 0, stream>>>(a.scores, a.total);
+    score_tc_kernel<<<grid, kThreads, L.total_bytes, stream>>>(tmap_a, tmap_q, p);
+    return cudaGetLastError() == cudaSuccess ? HSS_OK : HSS_ERR_CUDA;
 }
 
 }  // namespace hss

@@ -31,12 +31,44 @@ def ordered(b: np.ndarray) -> np.ndarray:
     return np.where(b & 0x8000, -mag, mag)
 
 
-def assert_bf16_within_ulp(gpu_bits, orc_bits, max_ulp: int = 1, what: str = ""):
-    d = np.abs(ordered(np.asarray(gpu_bits)) - ordered(np.asarray(orc_bits)))
-    worst = int(d.max()) if d.size else 0
+def bf16_ulp(b: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values at the magnitude of each bf16 pattern (subnormal floor 2^-133)."""
+    v = np.abs((np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32))
+    e = np.floor(np.log2(np.maximum(v.astype(np.float64), 2.0 ** -126)))
+    return 2.0 ** (np.maximum(e, -126) - 7)
+
+
+def abs_sum_scale(X_bits: np.ndarray, P_bits: np.ndarray) -> np.ndarray:
+    """sum_d |X_d| |P_dj| for every output of X . P (the size of the summed terms), in fp64."""
+    f = lambda b: (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+    return np.abs(f(X_bits).astype(np.float64)) @ np.abs(f(P_bits).astype(np.float64))
+
+
+def assert_bf16_within_ulp(gpu_bits, orc_bits, max_ulp: int = 1, what: str = "",
+                           scale=None, n_terms: int = 0):
+    """bf16 results within max_ulp of the oracle's.
+
+    Where `scale` (sum of |terms| of each output) is given, an output may instead lie within
+    1 ulp plus the fp32 accumulation bound 2 * n_terms * 2^-24 * scale: when the exact sum
+    nearly cancels, one bf16 step of the small result is finer than any fp32 accumulation
+    can resolve, for the GPU and for any other fp32 implementation alike.
+    """
+    g = np.asarray(gpu_bits)
+    o = np.asarray(orc_bits)
+    d = np.abs(ordered(g) - ordered(o))
+    bad = d > max_ulp
     n_off = int((d > 0).sum())
-    assert worst <= max_ulp, f"{what}: {n_off} of {d.size} differ, worst {worst} ulp"
-    return n_off
+    n_cancel = 0
+    if scale is not None and bad.any():
+        f = lambda b: (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        allow = bf16_ulp(o) + 2.0 * n_terms * 2.0 ** -24 * np.asarray(scale)
+        cancel = bad & (np.abs(f(g) - f(o)) <= allow)
+        n_cancel = int(cancel.sum())
+        bad = bad & ~cancel
+    worst = int(d.max()) if d.size else 0
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {d.size} beyond tolerance "
+                           f"({n_off} differ at all, worst {worst} ulp)")
+    return n_off, n_cancel
 
 
 def assert_scores_close(gpu: np.ndarray, orc: np.ndarray, tsum: np.ndarray, what: str = ""):
@@ -148,3 +180,13 @@ def oracle_slots(case, li: int, block_positions, nthreads: int | None = None):
                                   nthreads=nthreads or oracle.default_threads())
     assert st == 0
     return A[0]
+
+
+def slot_scale(case, li: int, block_positions) -> np.ndarray:
+    """sum_d |K_d| |P_dj| for the A_g slots of the given K blocks, slot layout [n, nkv, bs, r]."""
+    K = bits(case.K[li][torch.as_tensor(np.asarray(block_positions))])
+    return abs_sum_scale(K, bits(case.P)).transpose(0, 2, 1, 3)
+
+
+def q_scale(case, q_layer: int = 0) -> np.ndarray:
+    return abs_sum_scale(bits(case.Q[q_layer]), bits(case.P))

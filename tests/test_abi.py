@@ -68,6 +68,8 @@ def test_status_strings(lib):
     ({"num_q_heads": 30}, hss.HSS_ERR_INVALID_DIMS),    # 30 % 8 != 0 (PredictorDims::validate)
     ({"num_kv_heads": 0}, hss.HSS_ERR_INVALID_DIMS),
     ({"r": 24}, hss.HSS_ERR_UNSUPPORTED_SHAPE),
+    ({"r": 48}, hss.HSS_ERR_UNSUPPORTED_SHAPE),
+    ({"r": 256}, hss.HSS_ERR_UNSUPPORTED_SHAPE),
     ({"r": 512}, hss.HSS_ERR_UNSUPPORTED_SHAPE),
     ({"block_size": 8}, hss.HSS_ERR_UNSUPPORTED_SHAPE),
     ({"head_dim": 96}, hss.HSS_ERR_UNSUPPORTED_SHAPE),

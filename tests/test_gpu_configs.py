@@ -15,7 +15,7 @@ import kv_cache_block_lowrank_gb300 as hss
 import oracle
 import workloads as W
 from gpu_util import (SENTINEL, GpuRun, assert_bf16_within_ulp, assert_scores_close,
-                      assert_victims_match, bits, oracle_slots)
+                      assert_victims_match, bits, oracle_slots, q_scale, slot_scale)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -53,8 +53,10 @@ def test_tiny_end_to_end():
     Qp_o = oracle.project_q(bits(case.Q[0]), P)
     s_o, t_o, bad = oracle.score_blocks(Qp_o, A_o, 0, case.table.numpy(), offsets64(case))
     assert bad == 0
-    assert_bf16_within_ulp(bits(run.A), A_o, what="A_g")
-    assert_bf16_within_ulp(bits(Qp), Qp_o, what="Qp")
+    hd = d.head_dim
+    assert_bf16_within_ulp(bits(run.A)[0], A_o[0], what="A_g",
+                           scale=slot_scale(case, 0, np.arange(d.max_blocks)), n_terms=hd)
+    assert_bf16_within_ulp(bits(Qp), Qp_o, what="Qp", scale=q_scale(case), n_terms=hd)
     s_g = scores.cpu().numpy()
     assert_scores_close(s_g, s_o, t_o, "scores")
     assert_victims_match(vic.cpu().numpy(), s_o, t_o, offsets64(case), case.k_victims,
@@ -116,7 +118,8 @@ def test_decode_layer_full_size():
         pos = rng.choice(d.max_blocks, 24, replace=False)
         ids = case.block_ids.numpy()[pos]
         assert_bf16_within_ulp(bits(A_g[layer][torch.as_tensor(ids)]),
-                               oracle_slots(case, layer, pos), what=f"A_g layer {layer}")
+                               oracle_slots(case, layer, pos), what=f"A_g layer {layer}",
+                               scale=slot_scale(case, layer, pos), n_terms=d.head_dim)
     layer = 17
     Qp = run.project_q(layer)
     scores = run.score(Qp, layer)
@@ -127,7 +130,8 @@ def test_decode_layer_full_size():
     oracle.project_kv_blocks(bits(case.P), bits(case.K[layer]), 0, case.block_ids.numpy(), A_o,
                              nthreads=NT)
     Qp_o = oracle.project_q(bits(case.Q[layer]), bits(case.P))
-    assert_bf16_within_ulp(bits(Qp), Qp_o, what="Qp")
+    assert_bf16_within_ulp(bits(Qp), Qp_o, what="Qp", scale=q_scale(case, layer),
+                           n_terms=d.head_dim)
     s_o, t_o, _ = oracle.score_blocks(Qp_o, A_o, 0, case.table.numpy(), offsets64(case),
                                       nthreads=NT)
     s_g = scores.cpu().numpy()
@@ -152,7 +156,7 @@ def test_batched_decode_full_size():
     s_g = scores.cpu().numpy()
     v_g = vic.cpu().numpy()
     Qp_o = oracle.project_q(bits(case.Q[0]), bits(case.P))
-    assert_bf16_within_ulp(bits(Qp), Qp_o, what="Qp")
+    assert_bf16_within_ulp(bits(Qp), Qp_o, what="Qp", scale=q_scale(case), n_terms=d.head_dim)
     # Two whole sequences: every score and the victim set.
     for s in (0, 37):
         a, b = int(offs[s]), int(offs[s + 1])
@@ -193,9 +197,10 @@ def test_ingest_and_score_full_size():
     for layer in (0, L, 31):
         pos = rng.choice(len(new_ids), 16, replace=False)
         assert_bf16_within_ulp(bits(run.A[layer][torch.as_tensor(new_ids[pos])]),
-                               oracle_slots(case, layer, pos), what=f"A_g layer {layer}")
+                               oracle_slots(case, layer, pos), what=f"A_g layer {layer}",
+                               scale=slot_scale(case, layer, pos), n_terms=d.head_dim)
     Qp_o = oracle.project_q(bits(case.Q[0]), bits(case.P))
-    assert_bf16_within_ulp(bits(Qp), Qp_o, what="Qp")
+    assert_bf16_within_ulp(bits(Qp), Qp_o, what="Qp", scale=q_scale(case), n_terms=d.head_dim)
     # Sampled scores: the oracle projects each sampled block from its own K.
     table = case.table.numpy()
     where_new = {int(b): i for i, b in enumerate(new_ids)}
@@ -217,3 +222,29 @@ def test_ingest_and_score_full_size():
     v_g = vic.cpu().numpy()[0]
     exp = np.lexsort((np.arange(d.max_blocks), s_g))[:case.k_victims]
     assert np.array_equal(v_g, exp)
+
+
+def test_prefill_chunk_full_size():
+    """512 query rows x 64 heads against 8192 blocks (tensor-core path), bottom-1024."""
+    case = W.prefill(seed=0, device=DEV)
+    d = case.dims
+    run = GpuRun(case)
+    run.ingest(0, 0)
+    Qp = run.project_q(0)
+    scores = run.score(Qp, 0)            # auto: 4096 query vectors per kv head -> tcgen05
+    vic = run.rank(scores)
+    torch.cuda.synchronize()
+    assert int(run.status.item()) == 0 and hss.hss_read_device_error() == 0
+    Qp_o = oracle.project_q(bits(case.Q[0]), bits(case.P), nthreads=NT)
+    assert_bf16_within_ulp(bits(Qp), Qp_o, what="Qp", scale=q_scale(case), n_terms=d.head_dim)
+    rng = np.random.default_rng(4)
+    ent = rng.choice(d.max_blocks, 24, replace=False)
+    table = case.table.numpy()
+    A_o = np.zeros((1, d.max_blocks, d.num_kv_heads, d.block_size, d.r), dtype=np.uint16)
+    ids = table[ent]
+    A_o[0, ids] = oracle_slots(case, 0, ids)
+    s_o, t_o, _ = oracle.score_entries(Qp_o, A_o, 0, table, offsets64(case), ent)
+    s_g = scores.cpu().numpy()
+    assert_scores_close(s_g[ent], s_o, t_o, "sampled prefill scores")
+    exp = np.lexsort((np.arange(d.max_blocks), s_g))[:case.k_victims]
+    assert np.array_equal(vic.cpu().numpy()[0], exp)

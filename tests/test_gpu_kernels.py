@@ -10,7 +10,8 @@ import torch
 import kv_cache_block_lowrank_gb300 as hss
 import oracle
 import workloads as W
-from gpu_util import (SENTINEL, GpuRun, assert_bf16_within_ulp, assert_scores_close, bits)
+from gpu_util import (SENTINEL, GpuRun, abs_sum_scale, assert_bf16_within_ulp,
+                      assert_scores_close, bits)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -35,8 +36,8 @@ def dims(L=1, nq=8, nkv=2, hd=128, r=32, bs=16, B=64):
 
 # ----------------------------------------------------------------------------- projections
 
-@pytest.mark.parametrize("hd,r", [(64, 16), (128, 32), (128, 64), (256, 128), (64, 256),
-                                  (192, 48)])
+@pytest.mark.parametrize("hd,r", [(64, 16), (128, 32), (128, 64), (256, 128), (64, 128),
+                                  (192, 32)])
 def test_project_q(hd, r):
     g = gen(hd * 1000 + r)
     d = dims(nq=8, nkv=2, hd=hd, r=r)
@@ -47,7 +48,8 @@ def test_project_q(hd, r):
     hss.hss_project_q(d, P.to(DEV), Q.to(DEV), rows, Qp)
     torch.cuda.synchronize()
     ref = oracle.project_q(bits(Q), bits(P), nthreads=4)
-    assert_bf16_within_ulp(bits(Qp), ref, what="Qp")
+    assert_bf16_within_ulp(bits(Qp), ref, what="Qp", scale=abs_sum_scale(bits(Q), bits(P)),
+                           n_terms=hd)
 
 
 def test_project_q_single_row_decode_shape():
@@ -58,7 +60,8 @@ def test_project_q_single_row_decode_shape():
     Qp = torch.empty((1, 32, 32), dtype=torch.bfloat16, device=DEV)
     hss.hss_project_q(d, P.to(DEV), Q.to(DEV), 1, Qp)
     torch.cuda.synchronize()
-    assert_bf16_within_ulp(bits(Qp), oracle.project_q(bits(Q), bits(P)), what="Qp")
+    assert_bf16_within_ulp(bits(Qp), oracle.project_q(bits(Q), bits(P)), what="Qp",
+                           scale=abs_sum_scale(bits(Q), bits(P)), n_terms=128)
 
 
 @pytest.mark.parametrize("nkv,bs,r,n", [(2, 16, 32, 13), (8, 16, 32, 9), (8, 32, 64, 5),
@@ -79,7 +82,9 @@ def test_project_kv_blocks(nkv, bs, r, n):
     ref = np.zeros((1, B, nkv, bs, r), dtype=np.uint16)
     oracle.project_kv_blocks(bits(P), bits(K), 0, ids.numpy(), ref, nthreads=4)
     got = bits(A)
-    assert_bf16_within_ulp(got[layer][ids.numpy()], ref[0][ids.numpy()], what="A_g slots")
+    scale = abs_sum_scale(bits(K), bits(P)).transpose(0, 2, 1, 3)  # [n, nkv, bs, r]
+    assert_bf16_within_ulp(got[layer][ids.numpy()], ref[0][ids.numpy()], what="A_g slots",
+                           scale=scale, n_terms=hd)
     untouched = np.ones(B, dtype=bool)
     untouched[ids.numpy()] = False
     assert (got[layer][untouched] == SENTINEL).all(), "wrote a slot that was not addressed"
@@ -103,7 +108,8 @@ def test_project_kv_out_of_range_ids_are_skipped_and_reported():
     got = bits(A)[1]
     ref = np.zeros((1, 16, 8, 16, 32), dtype=np.uint16)
     oracle.project_kv_blocks(bits(P), bits(K[[0, 3]]), 0, np.array([3, 7]), ref)
-    assert_bf16_within_ulp(got[[3, 7]], ref[0][[3, 7]])
+    scale = abs_sum_scale(bits(K[[0, 3]]), bits(P)).transpose(0, 2, 1, 3)
+    assert_bf16_within_ulp(got[[3, 7]], ref[0][[3, 7]], scale=scale, n_terms=128)
     keep = np.ones(16, dtype=bool)
     keep[[3, 7]] = False
     assert (got[keep] == SENTINEL).all()
@@ -236,3 +242,76 @@ def test_rank_victims_all_equal():
     vic = torch.empty(1, k, dtype=torch.int32, device=DEV)
     hss.hss_rank_victims(s.to(DEV), offs.to(DEV), 1, n, k, vic)
     assert vic.cpu().numpy()[0].tolist() == list(range(k))
+
+
+# ----------------------------------------------------------------------------- tcgen05 scorer
+
+@pytest.mark.parametrize("nq,nkv,r,bs,rows,lengths", [
+    (64, 8, 64, 16, 40, [37]),           # 320 vectors per kv head: one full and one ragged chunk
+    (16, 4, 32, 16, 100, [0, 20, 9]),    # several sequences, one empty, ragged tiles
+    (8, 8, 128, 32, 600, [15]),          # g = 1, r = 128 (two K chunks), 2 slices of 512
+    (32, 2, 16, 16, 70, [11]),           # g = 16, r = 16 (32-byte swizzle), 1120 vectors
+    (32, 8, 32, 16, 1, [300]),           # the decode shape forced onto the tensor-core path
+    (64, 8, 64, 16, 512, [24]),          # the prefill chunk shape, few blocks
+])
+def test_score_tcgen05(nq, nkv, r, bs, rows, lengths):
+    g = gen(nq * 3 + nkv + r + bs + rows)
+    total = sum(lengths)
+    L, layer = 2, 1
+    B = max(total, 8) + 5
+    d = dims(L=L, nq=nq, nkv=nkv, hd=128, r=r, bs=bs, B=B)
+    A = synthetic_store(g, d, B)
+    S = len(lengths)
+    Qp = W.bf16_normal(g, (S, rows, nq, r))
+    table = torch.randperm(B, generator=g)[:total].to(torch.int32)
+    offs = W.identity_offsets(lengths)
+    scores = torch.full((total,), 7.0, dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    hss.hss_score_blocks(d, Qp.to(DEV), rows, A.to(DEV), layer, table.to(DEV), offs.to(DEV), S,
+                         total, scores, hss.HSS_PATH_TCGEN05, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and hss.hss_read_device_error() == 0
+    ref, tsum, bad = oracle.score_blocks(bits(Qp), bits(A), layer, table.numpy(),
+                                         offs.numpy().astype(np.int64), nthreads=8)
+    assert bad == 0
+    worst = assert_scores_close(scores.cpu().numpy(), ref, tsum, "tcgen05 scores")
+    assert worst < 1e-5
+
+
+def test_score_tcgen05_out_of_range_ids():
+    g = gen(31)
+    d = dims(L=1, nq=64, nkv=8, hd=128, r=64, bs=16, B=20)
+    A = synthetic_store(g, d, 20)
+    Qp = W.bf16_normal(g, (1, 64, 64, 64))
+    table = torch.tensor([0, 20, 5, -3, 19, 7, 8, 9, 10, 11], dtype=torch.int32)
+    offs = torch.tensor([0, 10], dtype=torch.int32)
+    scores = torch.empty(10, dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    hss.hss_score_blocks(d, Qp.to(DEV), 64, A.to(DEV), 0, table.to(DEV), offs.to(DEV), 1, 10,
+                         scores, hss.HSS_PATH_TCGEN05, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == hss.HSS_ERR_OUT_OF_RANGE
+    hss.hss_read_device_error()
+    ref, tsum, bad = oracle.score_blocks(bits(Qp), bits(A), 0, table.numpy(), np.array([0, 10]))
+    assert bad == 2
+    assert_scores_close(scores.cpu().numpy(), ref, tsum)
+
+
+def test_decode_and_tcgen05_paths_agree():
+    """Both kernels on the same decode-shaped inputs (each also checked against the oracle)."""
+    g = gen(41)
+    d = dims(L=1, nq=32, nkv=8, hd=128, r=32, bs=16, B=700)
+    A = synthetic_store(g, d, 700).to(DEV)
+    Qp = W.bf16_normal(g, (2, 2, 32, 32)).to(DEV)
+    table = torch.randperm(700, generator=g)[:650].to(torch.int32).to(DEV)
+    offs = torch.tensor([0, 300, 650], dtype=torch.int32, device=DEV)
+    out = []
+    for path in (hss.HSS_PATH_DECODE, hss.HSS_PATH_TCGEN05):
+        sc = torch.empty(650, dtype=torch.float32, device=DEV)
+        hss.hss_score_blocks(d, Qp, 2, A, 0, table, offs, 2, 650, sc, path)
+        out.append(sc)
+    torch.cuda.synchronize()
+    ref, tsum, _ = oracle.score_blocks(bits(Qp), bits(A), 0, table.cpu().numpy(),
+                                       offs.cpu().numpy().astype(np.int64), nthreads=8)
+    for sc in out:
+        assert_scores_close(sc.cpu().numpy(), ref, tsum)
