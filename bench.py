@@ -39,7 +39,8 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["hss", "reference"], default="hss")
-    p.add_argument("--workload", choices=["decode"], default="decode")
+    p.add_argument("--workload", choices=["decode", "batched", "prefill", "ingest"],
+                   default="decode")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -177,22 +178,39 @@ def measured_peaks():
             "source": "fallback"}
 
 
-# ----------------------------------------------------------------------------- decode workload
+# ----------------------------------------------------------------------------- workloads
 
-class DecodeWorkload:
+class _Base:
+    """Shared plumbing: binding handle, device buffers, graph-capturable steps."""
+
+    def __init__(self, device):
+        import torch
+
+        import kv_cache_block_lowrank_gb300 as hss
+
+        self.hss = hss
+        self.torch = torch
+        self.device = device
+
+    def slot_bytes(self):
+        d = self.dims
+        return d.num_kv_heads * d.block_size * d.r * 2
+
+    def score_bytes(self, n):
+        d = self.dims
+        return n * (self.slot_bytes() + 4 + 4) + d.num_q_heads * d.r * 2 + 8
+
+
+class DecodeWorkload(_Base):
     """The decode layer, all 32 layers projected; one step = 32 layer calls."""
 
     name = "decode"
 
     def __init__(self, device, seed: int):
-        import torch
-
-        import kv_cache_block_lowrank_gb300 as hss
+        super().__init__(device)
         import workloads as W
 
-        self.hss = hss
-        self.torch = torch
-        self.device = device
+        torch, hss = self.torch, self.hss
         self.case = c = W.decode(seed=seed, device=device)
         self.dims = d = c.dims
         self.L = d.num_layers
@@ -216,15 +234,8 @@ class DecodeWorkload:
         self.victims = torch.empty(self.L, 1, self.k, dtype=torch.int32, device=device)
         torch.cuda.synchronize()
 
-    # Work units and algorithmic bytes of the dominant kernel (the scorer).
     units_per_step = property(lambda self: self.L * self.n)
     launches_per_step = property(lambda self: self.L * 4)
-
-    @property
-    def score_bytes_per_launch(self):
-        d = self.dims
-        slot = d.num_kv_heads * d.block_size * d.r * 2
-        return self.n * (slot + 4 + 4) + d.num_q_heads * d.r * 2 + 8
 
     def layer_call(self, l: int, K_new=None, Q=None):
         hss, d = self.hss, self.dims
@@ -239,9 +250,16 @@ class DecodeWorkload:
         for l in range(self.L):
             self.layer_call(l)
 
-    def score_only(self, l: int):
-        self.hss.hss_score_blocks(self.dims, self.Qp[l], 1, self.A, l, self.table, self.offs, 1,
-                                  self.n, self.scores[l])
+    # The dominant kernel: the scorer, one launch per layer (32 cold layers per replay).
+    dominant_kernel = "score_decode"
+    dominant_bound = "hbm"
+    dominant_launches = property(lambda self: self.L)
+    dominant_units = property(lambda self: self.score_bytes(self.n))
+
+    def dominant(self):
+        for l in range(self.L):
+            self.hss.hss_score_blocks(self.dims, self.Qp[l], 1, self.A, l, self.table, self.offs,
+                                      1, self.n, self.scores[l])
 
     def describe(self):
         d = self.dims
@@ -250,6 +268,9 @@ class DecodeWorkload:
                 f"{d.block_size}, 1 sequence of {self.n * d.block_size} tokens ({self.n} blocks, "
                 f"permuted table), 1 query row, bottom-{self.k}; per layer call: project the "
                 f"block being written, project Q, score, rank")
+
+    l2_note = ("no flush: each step reads 32 x 16 MiB = 512 MiB of A_g, above the 129 MB L2, "
+               "so every layer call reads cold A_g")
 
     # ---- end to end through the API with host buffers
     def e2e_setup(self):
@@ -274,45 +295,348 @@ class DecodeWorkload:
         d2h = self.L * self.k * 4
         return h2d, d2h
 
+    def oracle_case(self, seed):
+        import workloads as W
+
+        return W.decode(seed=seed, device="cpu", layers=1)
+
+
+class BatchedWorkload(_Base):
+    """64 sequences over a 40000-block pool; one step = one layer call for the batch."""
+
+    name = "batched"
+
+    def __init__(self, device, seed: int):
+        super().__init__(device)
+        import workloads as W
+
+        torch, hss = self.torch, self.hss
+        self.case = c = W.batched(seed=seed, device=device)
+        self.dims = d = c.dims
+        self.S = c.num_seqs
+        self.n = c.total_blocks
+        self.k = c.k_victims
+        self.P = c.P.to(device)
+        self.A = torch.empty(d.a_g_shape, dtype=torch.bfloat16, device=device)
+        ids = c.block_ids.to(device)
+        hss.hss_project_kv_blocks(d, self.P, c.K[0], 0, ids, ids.numel(), self.A)
+        self.table = c.table.to(device)
+        self.offs = c.seq_offsets.to(device)
+        self.Q = c.Q[0]
+        self.Qp = torch.empty(self.S, 1, d.num_q_heads, d.r, dtype=torch.bfloat16, device=device)
+        self.scores = torch.empty(self.n, dtype=torch.float32, device=device)
+        self.victims = torch.empty(self.S, self.k, dtype=torch.int32, device=device)
+        torch.cuda.synchronize()
+
+    units_per_step = property(lambda self: self.n)
+    launches_per_step = 3
+
+    def step(self, Q=None):
+        hss, d = self.hss, self.dims
+        hss.hss_project_q(d, self.P, self.Q if Q is None else Q, self.S, self.Qp)
+        hss.hss_score_blocks(d, self.Qp, 1, self.A, 0, self.table, self.offs, self.S, self.n,
+                             self.scores)
+        hss.hss_rank_victims(self.scores, self.offs, self.S, self.n, self.k, self.victims)
+
+    dominant_kernel = "score_decode"
+    dominant_bound = "hbm"
+    dominant_launches = 1
+    dominant_units = property(lambda self: self.score_bytes(self.n))
+
+    def dominant(self):
+        self.hss.hss_score_blocks(self.dims, self.Qp, 1, self.A, 0, self.table, self.offs,
+                                  self.S, self.n, self.scores)
+
+    def describe(self):
+        return (f"batched decode: {self.S} sequences (contexts U{{1024..16384}} tokens, "
+                f"{self.n} blocks in all) from a 40000-block pool, 32 q / 8 kv heads, hd 128, "
+                f"r 32, bottom-{self.k} per sequence; per step: project Q, score, rank")
+
+    l2_note = "no flush: each step reads ~285 MB of A_g, above the 129 MB L2"
+
+    def e2e_setup(self):
+        torch = self.torch
+        self.h_Q = self.Q.cpu().pin_memory()
+        self.h_vic = torch.empty(self.S, self.k, dtype=torch.int32).pin_memory()
+        self.d_Q = torch.empty_like(self.Q)
+
+    def e2e_step(self):
+        self.d_Q.copy_(self.h_Q, non_blocking=True)
+        self.step(Q=self.d_Q)
+        self.h_vic.copy_(self.victims, non_blocking=True)
+        self.torch.cuda.current_stream().synchronize()
+
+    @property
+    def e2e_bytes(self):
+        return self.Q.numel() * 2, self.S * self.k * 4
+
+
+class PrefillWorkload(_Base):
+    """A 512-row prefill chunk against 8192 blocks (tcgen05 scorer).  Two copies of the
+    context's A_g alternate between steps so each step reads it cold (2 x 128 MiB > L2)."""
+
+    name = "prefill"
+
+    def __init__(self, device, seed: int):
+        super().__init__(device)
+        import workloads as W
+
+        torch, hss = self.torch, self.hss
+        self.case = c = W.prefill(seed=seed, device=device)
+        base = c.dims
+        self.dims = d = W.Dims(2, base.num_q_heads, base.num_kv_heads, base.head_dim, base.r,
+                               base.block_size, base.max_blocks)
+        self.n = c.total_blocks
+        self.k = c.k_victims
+        self.R = c.rows_per_seq
+        self.P = c.P.to(device)
+        self.A = torch.empty(d.a_g_shape, dtype=torch.bfloat16, device=device)
+        ids = c.block_ids.to(device)
+        for layer in range(2):
+            hss.hss_project_kv_blocks(d, self.P, c.K[0], layer, ids, ids.numel(), self.A)
+        self.table = c.table.to(device)
+        self.offs = c.seq_offsets.to(device)
+        # The chunk's own keys: its 512 tokens are the last 32 blocks of the table.
+        nb = self.R // d.block_size
+        self.new_ids = self.table[-nb:].contiguous()
+        self.K_new = c.K[0][self.new_ids.long()].contiguous()
+        self.Q = c.Q[0]
+        self.Qp = torch.empty(1, self.R, d.num_q_heads, d.r, dtype=torch.bfloat16, device=device)
+        self.scores = torch.empty(2, self.n, dtype=torch.float32, device=device)
+        self.victims = torch.empty(2, 1, self.k, dtype=torch.int32, device=device)
+        self.parity = 0
+        torch.cuda.synchronize()
+
+    units_per_step = property(lambda self: self.n)
+    launches_per_step = 5  # ingest, project Q, fill, score, rank
+
+    def step(self, Q=None, K_new=None):
+        hss, d, l = self.hss, self.dims, self.parity
+        hss.hss_project_kv_blocks(d, self.P, self.K_new if K_new is None else K_new, l,
+                                  self.new_ids, self.new_ids.numel(), self.A)
+        hss.hss_project_q(d, self.P, self.Q if Q is None else Q, self.R, self.Qp)
+        hss.hss_score_blocks(d, self.Qp, self.R, self.A, l, self.table, self.offs, 1, self.n,
+                             self.scores[l])
+        hss.hss_rank_victims(self.scores[l], self.offs, 1, self.n, self.k, self.victims[l])
+        self.parity ^= 1
+
+    def steps_for_graph(self):
+        # A graph holds both parities so replays alternate the A_g copy.
+        self.step()
+        self.step()
+
+    graph_steps = 2
+    dominant_kernel = "score_tc"
+    dominant_bound = "tensor"
+    dominant_launches = 2
+
+    @property
+    def dominant_units(self):
+        d = self.dims
+        return 2.0 * self.R * d.num_q_heads * d.block_size * d.r * self.n  # flop per launch
+
+    def dominant(self):
+        for l in range(2):
+            self.hss.hss_score_blocks(self.dims, self.Qp, self.R, self.A, l, self.table,
+                                      self.offs, 1, self.n, self.scores[l])
+
+    def describe(self):
+        d = self.dims
+        return (f"prefill chunk: {self.R} query rows x {d.num_q_heads} q heads (g "
+                f"{d.num_q_heads // d.num_kv_heads}) against {self.n} blocks "
+                f"({self.n * d.block_size} tokens), hd {d.head_dim}, r {d.r}, bottom-{self.k}; "
+                f"per step: project the chunk's {self.new_ids.numel()} blocks, project Q, "
+                f"score (tcgen05), rank")
+
+    l2_note = ("no flush: steps alternate between two 128 MiB copies of the context's A_g "
+               "(256 MiB > 129 MB L2)")
+
+    def e2e_setup(self):
+        torch = self.torch
+        self.h_Q = self.Q.cpu().pin_memory()
+        self.h_K = self.K_new.cpu().pin_memory()
+        self.h_vic = torch.empty(self.k, dtype=torch.int32).pin_memory()
+        self.d_Q = torch.empty_like(self.Q)
+        self.d_K = torch.empty_like(self.K_new)
+
+    def e2e_step(self):
+        self.d_Q.copy_(self.h_Q, non_blocking=True)
+        self.d_K.copy_(self.h_K, non_blocking=True)
+        l = self.parity
+        self.step(Q=self.d_Q, K_new=self.d_K)
+        self.h_vic.copy_(self.victims[l][0], non_blocking=True)
+        self.torch.cuda.current_stream().synchronize()
+
+    @property
+    def e2e_bytes(self):
+        return self.Q.numel() * 2 + self.K_new.numel() * 2, self.k * 4
+
+
+class IngestWorkload(_Base):
+    """4096 new blocks projected into each of 32 layers, then one layer's 65536 blocks
+    scored and ranked; skewed keys.  One step = 32 ingest calls + project Q + score + rank."""
+
+    name = "ingest"
+
+    def __init__(self, device, seed: int):
+        super().__init__(device)
+        import workloads as W
+
+        torch, hss = self.torch, self.hss
+        self.case = c = W.ingest(seed=seed, device=device)
+        self.dims = d = c.dims
+        self.L = d.num_layers
+        self.n = c.total_blocks
+        self.k = c.k_victims
+        self.P = c.P.to(device)
+        self.A = torch.empty(d.a_g_shape, dtype=torch.bfloat16, device=device)
+        self.new_ids = c.block_ids.to(device)
+        self.K = c.K
+        self.layer = c.score_layer
+        fill = c.fill_ids.to(device)
+        hss.hss_project_kv_blocks(d, self.P, c.K_fill, self.layer, fill, fill.numel(), self.A)
+        self.table = c.table.to(device)
+        self.offs = c.seq_offsets.to(device)
+        self.Q = c.Q[0]
+        self.Qp = torch.empty(1, 1, d.num_q_heads, d.r, dtype=torch.bfloat16, device=device)
+        self.scores = torch.empty(self.n, dtype=torch.float32, device=device)
+        self.victims = torch.empty(1, self.k, dtype=torch.int32, device=device)
+        torch.cuda.synchronize()
+
+    units_per_step = property(lambda self: self.n)
+    launches_per_step = property(lambda self: self.L + 3)
+
+    def step(self):
+        hss, d = self.hss, self.dims
+        nb = self.new_ids.numel()
+        for l in range(self.L):
+            hss.hss_project_kv_blocks(d, self.P, self.K[l], l, self.new_ids, nb, self.A)
+        hss.hss_project_q(d, self.P, self.Q, 1, self.Qp)
+        hss.hss_score_blocks(d, self.Qp, 1, self.A, self.layer, self.table, self.offs, 1, self.n,
+                             self.scores)
+        hss.hss_rank_victims(self.scores, self.offs, 1, self.n, self.k, self.victims)
+
+    dominant_kernel = "project (ingest)"
+    dominant_bound = "hbm"
+    dominant_launches = property(lambda self: self.L)
+
+    @property
+    def dominant_units(self):
+        d = self.dims
+        nb = self.new_ids.numel()
+        return nb * d.block_size * d.num_kv_heads * (d.head_dim * 2 + d.r * 2) + d.head_dim * d.r * 2
+
+    def dominant(self):
+        nb = self.new_ids.numel()
+        for l in range(self.L):
+            self.hss.hss_project_kv_blocks(self.dims, self.P, self.K[l], l, self.new_ids, nb,
+                                           self.A)
+
+    def describe(self):
+        return (f"ingest + score under skew: {self.new_ids.numel()} new blocks projected into "
+                f"each of {self.L} layers (K with 4 outlier channels x20 and log-normal token "
+                f"norms), then layer {self.layer}'s {self.n} blocks scored, bottom-{self.k}")
+
+    l2_note = "no flush: each step reads 4 GiB of K and 512 MiB of A_g, far above the 129 MB L2"
+
+    def e2e_setup(self):
+        self.h_vic = self.torch.empty(1, self.k, dtype=self.torch.int32).pin_memory()
+
+    def e2e_step(self):
+        self.step()
+        self.h_vic.copy_(self.victims, non_blocking=True)
+        self.torch.cuda.current_stream().synchronize()
+
+    @property
+    def e2e_bytes(self):
+        return 0, self.k * 4
+
+
+WORKLOADS = {"decode": DecodeWorkload, "batched": BatchedWorkload, "prefill": PrefillWorkload,
+             "ingest": IngestWorkload}
+
 
 # ----------------------------------------------------------------------------- oracle timing
 
-def oracle_decode_sample(case, max_seconds: float, nthreads: int, blocks_per_call=None,
-                         max_calls=None):
-    """Time the oracle on decode layer calls; returns (blocks scored, seconds, calls, blocks)."""
+def _bits(t):
     import numpy as np
+    import torch
 
-    import oracle
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
-    def bits(t):
-        return t.detach().cpu().contiguous().view(__import__("torch").int16).numpy().view(
-            np.uint16)
 
-    d = case.dims
-    layer = 0
-    n = case.total_blocks if blocks_per_call is None else min(blocks_per_call, case.total_blocks)
-    table = case.table.numpy()[:n].astype(np.int32)
-    P = bits(case.P)
-    K = bits(case.K[layer])
-    A = np.zeros((1, d.max_blocks, d.num_kv_heads, d.block_size, d.r), dtype=np.uint16)
-    ids = table  # pool position == block id in this workload
-    oracle.project_kv_blocks(P, K[ids], 0, ids, A, nthreads=nthreads)  # context (untimed)
-    Q = bits(case.Q[layer])
-    offs = np.array([0, n], dtype=np.int64)
-    new = np.array([int(case.table[-1])], dtype=np.int32)
-    Knew = K[new]
-    calls, scored = 0, 0
-    t0 = time.perf_counter()
-    while True:
-        oracle.project_kv_blocks(P, Knew, 0, new, A, nthreads=nthreads)
-        Qp = oracle.project_q(Q, P, nthreads=nthreads)
-        s, _, _ = oracle.score_blocks(Qp, A, 0, table, offs, nthreads=nthreads)
-        oracle.rank_victims(s.astype(np.float32), offs, min(case.k_victims, n))
-        calls += 1
-        scored += n
-        el = time.perf_counter() - t0
-        if el >= max_seconds or (max_calls is not None and calls >= max_calls):
-            return scored, el, calls, n
+SAMPLE_BLOCKS = {"decode": 2048, "batched": 544, "prefill": 8, "ingest": 256}
+
+
+class OracleSample:
+    """The CPU oracle on a sample of one workload's step, in the GPU step's proportions.
+
+    Each call projects the query rows, projects `ingest_per_block` new blocks per scored
+    block (the decode workloads project one block per layer call; the ingest workload two
+    per scored block), scores `m` table entries and ranks them.  Unit: blocks scored/s.
+    """
+
+    def __init__(self, name: str, seed: int, threads: int):
+        import numpy as np
+
+        import oracle
+        import workloads as W
+
+        self.np, self.oracle, self.threads = np, oracle, threads
+        one = lambda d: W.Dims(1, d.num_q_heads, d.num_kv_heads, d.head_dim, d.r, d.block_size,
+                               d.max_blocks)
+        # (dims, query rows, key distribution, blocks drawn, ingest per call, ingest per scored)
+        spec = {"decode": (one(W.DECODE), 1, "normal", 2048, 1, 0.0),
+                "batched": (W.BATCHED, 1, "normal", 1024, 0, 0.0),
+                "prefill": (W.PREFILL, 512, "normal", 64, 32, 0.0),
+                "ingest": (one(W.INGEST), 1, "skewed", 1024, 0, 2.0)}[name]
+        dims, rows, kind, pool, self.extra_ingest, self.ingest_ratio = spec
+        m = SAMPLE_BLOCKS[name]
+        c = W.generic(name, dims, num_seqs=1, rows_per_seq=rows, lengths=[min(m, pool)],
+                      k_victims={"decode": 256, "batched": 64, "prefill": 1024,
+                                 "ingest": 4096}[name],
+                      seed=seed, key_kind=kind, pool=pool)
+        self.case = c
+        d = c.dims
+        self.P = _bits(c.P)
+        self.Q = _bits(c.Q[0])
+        self.K = _bits(c.K[0])
+        self.table = c.table.numpy()
+        self.pool = self.K.shape[0]
+        self.A = np.zeros((1, d.max_blocks, d.num_kv_heads, d.block_size, d.r), dtype=np.uint16)
+
+    def call(self, m: int):
+        """One sampled call scoring m entries; returns m."""
+        np, oracle, c = self.np, self.oracle, self.case
+        ids = (self.table[:m] % self.pool).astype(np.int32)
+        n_ing = self.extra_ingest + int(round(self.ingest_ratio * m))
+        if n_ing > 0:
+            pos = np.arange(n_ing) % self.pool
+            oracle.project_kv_blocks(self.P, self.K[pos], 0, ids[pos % m] if m else pos.astype(
+                np.int32), self.A, nthreads=self.threads)
+        Qp = oracle.project_q(self.Q, self.P, nthreads=self.threads)
+        offs = np.array([0, m], dtype=np.int64)
+        s, _, _ = oracle.score_blocks(Qp, self.A, 0, ids, offs, nthreads=self.threads)
+        oracle.rank_victims(s.astype(np.float32), offs, max(1, min(c.k_victims, m)))
+        return m
+
+    def prepare(self, m: int):
+        """Project the sampled blocks' context (untimed)."""
+        ids = (self.table[:m] % self.pool).astype(self.np.int32)
+        pos = self.np.arange(m) % self.pool
+        self.oracle.project_kv_blocks(self.P, self.K[pos], 0, ids, self.A,
+                                      nthreads=self.threads)
+
+    def time(self, m: int, seconds: float, max_calls=None):
+        self.prepare(m)
+        calls, scored = 0, 0
+        t0 = time.perf_counter()
+        while True:
+            scored += self.call(m)
+            calls += 1
+            el = time.perf_counter() - t0
+            if el >= seconds or (max_calls is not None and calls >= max_calls):
+                return scored, el, calls
 
 
 def cpu_threads():
@@ -322,28 +646,29 @@ def cpu_threads():
         return os.cpu_count() or 1
 
 
+
+
 # ----------------------------------------------------------------------------- arms
 
 def run_reference(args):
     rank, world, local = dist_env()
     if rank != 0:
         return 0
-    import workloads as W
-
-    case = W.decode(seed=args.seed, device="cpu", layers=1)
     threads = cpu_threads()
+    orc = OracleSample(args.workload, args.seed, threads)
+    m_full = SAMPLE_BLOCKS[args.workload]
     # Per-block cost, to size each step's sample so the whole run takes about a minute.
-    scored, el, _, _ = oracle_decode_sample(case, 0.0, threads, blocks_per_call=64, max_calls=1)
+    scored, el, _ = orc.time(min(16, m_full), 0.0, max_calls=1)
     per_block = el / max(scored, 1)
     total_steps = args.steps + args.warmup
-    sample = int(max(16, min(case.total_blocks, 60.0 / max(total_steps * per_block, 1e-12))))
+    m = int(max(1, min(m_full, 60.0 / max(total_steps * per_block, 1e-12))))
+    orc.prepare(m)
     for _ in range(args.warmup):
-        oracle_decode_sample(case, 0.0, threads, blocks_per_call=sample, max_calls=1)
+        orc.call(m)
     t0 = time.perf_counter()
     blocks = 0
     for _ in range(args.steps):
-        b, _, _, _ = oracle_decode_sample(case, 0.0, threads, blocks_per_call=sample, max_calls=1)
-        blocks += b
+        blocks += orc.call(m)
     el = time.perf_counter() - t0
     value = blocks / el
     line = {
@@ -351,10 +676,9 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "decode layer call (oracle): project the new block, project Q, "
-                               f"score the first {sample} blocks of the table, rank"},
+        "config": {"workload": f"{args.workload} (CPU oracle, {m} blocks scored per step)"},
         "cpu_baseline": {"value": value, "unit": "blocks/s", "cores": threads, "kind": "oracle",
-                         "sample": f"{args.steps} layer calls of {sample} blocks each"},
+                         "sample": f"{args.steps} sampled {args.workload} calls of {m} blocks"},
         "e2e": {"value": value, "unit": "blocks/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -376,25 +700,29 @@ def run_hss(args):
     __graft_entry__.build()
     import kv_cache_block_lowrank_gb300 as hss
 
-    wl = DecodeWorkload(device, args.seed + rank)
+    wl = WORKLOADS[args.workload](device, args.seed + rank)
     peaks = measured_peaks()
     stream = torch.cuda.Stream(device=device)
     torch.cuda.synchronize()
+    per_replay = getattr(wl, "graph_steps", 1)
+    capture = getattr(wl, "steps_for_graph", wl.step)
 
-    # ---- warm-up, then capture one step into a CUDA graph
+    # ---- warm-up, then capture the step into a CUDA graph
     with torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 3)):
-            wl.step()
+            capture()
     stream.synchronize()
     graph = None
     if not args.no_graph:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
-            wl.step()
+            capture()
         for _ in range(3):
             graph.replay()
         torch.cuda.synchronize()
-    run_step = graph.replay if graph is not None else wl.step
+    run_replay = graph.replay if graph is not None else capture
+    replays = max(1, args.steps // per_replay)
+    steps = replays * per_replay
 
     # ---- timed region
     ev0 = torch.cuda.Event(enable_timing=True)
@@ -404,22 +732,21 @@ def run_hss(args):
     with ClockSampler(device_uuid(local)) as clocks:
         with torch.cuda.stream(stream):
             ev0.record(stream)
-            for _ in range(args.steps):
-                run_step()
+            for _ in range(replays):
+                run_replay()
             ev1.record(stream)
         stream.synchronize()
     torch.cuda.synchronize()
     barrier(world, device)
     elapsed = ev0.elapsed_time(ev1) / 1e3
-    elapsed_max, units = aggregate(elapsed, wl.units_per_step * args.steps, world, device)
+    elapsed_max, units = aggregate(elapsed, wl.units_per_step * steps, world, device)
     value = units / elapsed_max
 
-    # ---- dominant kernel (the scorer): 32 back-to-back launches (cold layers) per replay
+    # ---- dominant kernel: graphs of back-to-back launches timed with events on its stream
     reps = max(20, min(400, args.steps // 4))
     g2 = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g2, stream=stream):
-        for l in range(wl.L):
-            wl.score_only(l)
+        wl.dominant()
     with torch.cuda.stream(stream):
         for _ in range(3):
             g2.replay()
@@ -430,28 +757,34 @@ def run_hss(args):
             g2.replay()
         e1.record(stream)
     stream.synchronize()
-    score_s = e0.elapsed_time(e1) / 1e3 / (reps * wl.L)
-    achieved = wl.score_bytes_per_launch / score_s / 1e9
+    dom_s = e0.elapsed_time(e1) / 1e3 / (reps * wl.dominant_launches)
+    if wl.dominant_bound == "hbm":
+        achieved, peak, unit = wl.dominant_units / dom_s / 1e9, peaks["hbm_gbs"], "GB/s"
+        peak_src = peaks["source"] + " hbm_gbs (copy)"
+    else:
+        achieved, peak, unit = wl.dominant_units / dom_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+        peak_src = peaks["source"] + " bf16_tflops (burst, cuBLAS)"
 
     # ---- end to end through the API with host buffers
     e2e = None
     if args.e2e_steps > 0:
         wl.e2e_setup()
+        n_e2e = max(1, args.e2e_steps // per_replay) * per_replay
         with torch.cuda.stream(stream):
-            for _ in range(3):
+            for _ in range(3 * per_replay):
                 wl.e2e_step()
             torch.cuda.synchronize()
             barrier(world, device)
             t0 = time.perf_counter()
-            for _ in range(args.e2e_steps):
+            for _ in range(n_e2e):
                 wl.e2e_step()
             t1 = time.perf_counter()
-        el_e2e, units_e2e = aggregate(t1 - t0, wl.units_per_step * args.e2e_steps, world, device)
+        el_e2e, units_e2e = aggregate(t1 - t0, wl.units_per_step * n_e2e, world, device)
         h2d, d2h = wl.e2e_bytes
         e2e = {"value": units_e2e / el_e2e, "unit": "blocks/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-               "how": "every layer call from the host through the C ABI (no graph): pinned "
-                      "H2D of Q and the new K block, D2H of the victims, one sync per step"}
+               "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "how": "every call from the host through the C ABI (no graph): pinned H2D of the "
+                      "step's new inputs, D2H of the victims, one sync per step"}
 
     err = hss.hss_read_device_error()
     if err != 0:
@@ -459,41 +792,35 @@ def run_hss(args):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        import workloads as W
-
         threads = cpu_threads()
-        case_cpu = W.decode(seed=args.seed, device="cpu", layers=1)
-        scored, el, calls, n = oracle_decode_sample(case_cpu, 10.0, threads)
+        orc = OracleSample(args.workload, args.seed, threads)
+        m = SAMPLE_BLOCKS[args.workload]
+        scored, el, calls = orc.time(m, 10.0)
         cpu = {"value": scored / el, "unit": "blocks/s", "cores": threads, "kind": "oracle",
-               "sample": f"{calls} decode layer calls ({n} blocks each: project the new block, "
-                         f"project Q, score, rank) on layer 0, ~10 s"}
+               "sample": f"{calls} oracle calls on the {args.workload} workload, {m} blocks "
+                         f"scored per call in the GPU step's proportions, ~10 s"}
 
     if rank == 0:
-        d = wl.dims
-        slot = d.num_kv_heads * d.block_size * d.r * 2
+        slot = wl.slot_bytes()
         line = {
             "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": elapsed_max / args.steps * 1e3, "higher_is_better": True,
+            "steps": steps, "warmup": args.warmup,
+            "ms_per_step": elapsed_max / steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "a_g_gbs": value * slot / 1e9,
             "a_g_hbm_frac": value * slot / 1e9 / peaks["hbm_gbs"],
-            "config": {"workload": wl.describe(),
-                       "l2": "no flush: each step reads 32 x 16 MiB = 512 MiB of A_g, above "
-                             "the 129 MB L2, so every layer call reads cold A_g",
-                       "graph": graph is not None, "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "hbm", "kernel": "score_decode", "achieved": achieved,
-                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": achieved / peaks["hbm_gbs"], "traffic": None,
-                         "peak_source": peaks["source"] + " hbm_gbs (burst copy)",
-                         "launch_us": score_s * 1e6,
-                         "bytes_per_launch": wl.score_bytes_per_launch,
-                         "how": "CUDA events around graphs of 32 back-to-back scorer launches "
-                                "(one per layer) on the launching stream; duration per launch "
-                                "includes the gap between graph nodes"},
+            "config": {"workload": wl.describe(), "l2": wl.l2_note, "graph": graph is not None,
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": wl.dominant_bound, "kernel": wl.dominant_kernel,
+                         "achieved": achieved, "peak": peak, "unit": unit,
+                         "frac": achieved / peak, "traffic": None, "peak_source": peak_src,
+                         "launch_us": dom_s * 1e6, "work_per_launch": wl.dominant_units,
+                         "how": "CUDA events around graph replays of back-to-back launches of "
+                                "this kernel on its launching stream (gaps between graph nodes "
+                                "included)"},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": wl.launches_per_step * args.steps,
+            "gpu_launches": wl.launches_per_step * steps,
             "clocks": clocks.summary(),
         }
         print(json.dumps(line), flush=True)

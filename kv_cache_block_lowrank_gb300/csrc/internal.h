@@ -24,6 +24,25 @@ struct DeviceInfo {
 // Returns the info of the current device, initialising it on first use.  nullptr on failure.
 const DeviceInfo* current_device_info();
 
+// Launch with programmatic stream serialization: the kernel may be scheduled while the
+// previous kernel in the stream finishes; it waits for it (griddepcontrol.wait) before
+// touching global memory, so only launch latency and on-chip set-up overlap.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // ------------------------------------------------------------------- projection (tcgen05)
 // Y rows = bf16(X rows . P).  X is [num_rows, head_dim] bf16.  Output row m goes to
 //   - Qp mode (block_ids == nullptr): out + m * r

@@ -98,14 +98,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = p.r;
     const int64_t num_tiles = (p.num_rows + kBM - 1) / kBM;
 
-    // P^T into shared memory, K-major with the 128-byte swizzle the MMA descriptor names:
-    // row j of chunk c holds P[64c .. 64c+63][j].
-    for (int e = threadIdx.x; e < p.head_dim * r; e += kThreads) {
-        const int d = e / r, j = e - (e / r) * r;
-        const uint16_t v = p.P[e];
-        const int c = d / kChunkElems, kk = d - c * kChunkElems;
-        *reinterpret_cast<uint16_t*>(sB + c * r * 128 + swizzled_offset(j, kk * 2, 128)) = v;
-    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
@@ -118,11 +110,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         fence_mbarrier_init();
     }
-    fence_proxy_async_smem();  // make the generic-proxy P^T writes visible to the tensor cores
     if (warp == 1) {
         tmem_alloc(tmem_slot, L.tmem_cols);
         tmem_relinquish();
     }
+    // Everything above is set-up that may overlap the previous kernel in the stream; global
+    // memory is touched only after the dependency wait.
+    grid_dependency_wait();
+    grid_launch_dependents();
+    // P^T into shared memory, K-major with the 128-byte swizzle the MMA descriptor names:
+    // row j of chunk c holds P[64c .. 64c+63][j].  P is read with 16-byte loads, a batch of
+    // four per thread in flight at once, then scattered into the transposed layout.
+    {
+        const int n16 = p.head_dim * r / 8;  // 16-byte chunks of P (8 consecutive j each)
+        const uint4* P16 = reinterpret_cast<const uint4*>(p.P);
+        for (int base = threadIdx.x; base < n16; base += 4 * kThreads) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = base + u * kThreads;
+                if (e < n16) v[u] = __ldg(&P16[e]);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = base + u * kThreads;
+                if (e >= n16) continue;
+                const int d = (e * 8) / r, j0 = (e * 8) - d * r;
+                const int c = d / kChunkElems, kk = d - c * kChunkElems;
+                uint8_t* chunk = sB + c * r * 128;
+                const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint16_t h = static_cast<uint16_t>(w[q >> 1] >> (16 * (q & 1)));
+                    *reinterpret_cast<uint16_t*>(chunk + swizzled_offset(j0 + q, kk * 2, 128)) = h;
+                }
+            }
+        }
+    }
+    fence_proxy_async_smem();  // make the generic-proxy P^T writes visible to the tensor cores
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -348,8 +373,11 @@ hss_status launch_project(const ProjectArgs& a, cudaStream_t stream) {
     p.lib_error = dev->error_word;
     const int64_t num_tiles = (a.num_rows + kBM - 1) / kBM;
     const int grid = static_cast<int>(std::min<int64_t>(num_tiles, dev->num_sms));
-    project_kernel<<<grid, kThreads, L.total_bytes, stream>>>(tmap, p, L.stages);
-    return cudaGetLastError() == cudaSuccess ? HSS_OK : HSS_ERR_CUDA;
+    const int stages = L.stages;
+    if (launch_pdl(project_kernel, dim3(grid), dim3(kThreads), L.total_bytes, stream, tmap, p,
+                   stages) != cudaSuccess)
+        return HSS_ERR_CUDA;
+    return HSS_OK;
 }
 
 }  // namespace hss

@@ -37,6 +37,22 @@ __device__ __forceinline__ uint32_t lane_id() {
 }
 
 // ---------------------------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel here is launched with programmatic stream
+// serialization, so it may start while the previous kernel in the stream is finishing.
+// grid_dependency_wait() blocks until that kernel has completed and its memory is visible;
+// each kernel calls it before its first global-memory access.  grid_launch_dependents()
+// lets the next kernel start its own launch and set-up early.  Both are no-ops when the
+// kernel was launched without the attribute.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

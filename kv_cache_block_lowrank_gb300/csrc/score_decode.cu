@@ -90,6 +90,8 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
 
     const int64_t wid = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + warp;
     const int64_t i_begin = wid * p.entries_per_warp;
+    grid_dependency_wait();
+    grid_launch_dependents();
     if (i_begin >= p.total) return;
     const int64_t i_end = min(p.total, i_begin + p.entries_per_warp);
 
@@ -125,31 +127,6 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
             while (i >= seq_end && s + 1 < p.num_seqs) {
                 ++s;
                 seq_end = __ldg(&p.seq_offsets[s + 1]);
-            }
-            if (s != cached_seq) {
-                // Query-vector fragments of sequence s, in MMA B-fragment order.
-                __syncwarp();
-                for (int c = 0; c < p.nkv; ++c) {
-#pragma unroll
-                    for (int ks = 0; ks < KSTEPS; ++ks) {
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            const int v = nt * 8 + gq;
-                            uint2 f = make_uint2(0u, 0u);
-                            if (v < p.nvec) {
-                                const int row = v / p.g;
-                                const int h = c * p.g + (v - row * p.g);
-                                const uint16_t* q =
-                                    p.Qp + ((static_cast<int64_t>(s) * p.rows + row) * p.nq + h) *
-                                               p.r;
-                                f = *reinterpret_cast<const uint2*>(q + frag_r_offset<KSTEPS>(ks, tq));
-                            }
-                            cache[((c * KSTEPS + ks) * NT + nt) * 32 + lane] = f;
-                        }
-                    }
-                }
-                __syncwarp();
-                cached_seq = s;
             }
             const int32_t id = __shfl_sync(0xffffffffu, my_id, e);
             if (id < 0 || id >= p.max_blocks) {
@@ -189,6 +166,32 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
                             }
                         }
                     }
+                }
+                // (Re)fill the query-vector fragment cache while the loads are in flight.
+                if (s != cached_seq) {
+                    // Query-vector fragments of sequence s, in MMA B-fragment order.
+                    __syncwarp();
+                    for (int c = 0; c < p.nkv; ++c) {
+#pragma unroll
+                        for (int ks = 0; ks < KSTEPS; ++ks) {
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                const int v = nt * 8 + gq;
+                                uint2 f = make_uint2(0u, 0u);
+                                if (v < p.nvec) {
+                                    const int row = v / p.g;
+                                    const int h = c * p.g + (v - row * p.g);
+                                    const uint16_t* q =
+                                        p.Qp + ((static_cast<int64_t>(s) * p.rows + row) * p.nq + h) *
+                                                   p.r;
+                                    f = *reinterpret_cast<const uint2*>(q + frag_r_offset<KSTEPS>(ks, tq));
+                                }
+                                cache[((c * KSTEPS + ks) * NT + nt) * 32 + lane] = f;
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    cached_seq = s;
                 }
 #pragma unroll
                 for (int u = 0; u < kTilesPerBatch; ++u) {
@@ -245,8 +248,9 @@ hss_status launch_t(const DecodeParams& p, int warps_per_cta, int smem, int grid
             cudaSuccess)
             return HSS_ERR_CUDA;
     }
-    k<<<grid, warps_per_cta * 32, smem, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? HSS_OK : HSS_ERR_CUDA;
+    if (launch_pdl(k, dim3(grid), dim3(warps_per_cta * 32), smem, stream, p) != cudaSuccess)
+        return HSS_ERR_CUDA;
+    return HSS_OK;
 }
 
 int frag_bytes_per_warp(const ScoreArgs& a) {

@@ -133,6 +133,8 @@ __device__ __forceinline__ void atomic_max_f32(float* addr, float v) {
 }
 
 __global__ void fill_neg_inf(float* __restrict__ x, int64_t n) {
+    grid_dependency_wait();
+    grid_launch_dependents();
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x)
         x[i] = -INFINITY;
@@ -161,6 +163,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     constexpr uint32_t kTmemCols = 512;
 
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    grid_dependency_wait();
+    grid_launch_dependents();
     // Units before each sequence: nkv * nslices * tiles(s) per sequence.
     if (threadIdx.x == 0) {
         int64_t acc = 0;
@@ -182,10 +190,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         *abort_flag = 0;
         fence_mbarrier_init();
-    }
-    if (warp == 1) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -502,9 +506,15 @@ hss_status launch_score_tc(const ScoreArgs& a, cudaStream_t stream) {
     p.units_per_cta = (p.total_units + grid - 1) / grid;
 
     const int fill_grid = static_cast<int>(std::min<int64_t>((a.total + 255) / 256, 1024));
-    fill_neg_inf<<<fill_grid, 256, 0, stream>>>(a.scores, a.total);
-    score_tc_kernel<<<grid, kThreads, L.total_bytes, stream>>>(tmap_a, tmap_q, p);
-    return cudaGetLastError() == cudaSuccess ? HSS_OK : HSS_ERR_CUDA;
+    float* scores = a.scores;
+    const int64_t total = a.total;
+    if (launch_pdl(fill_neg_inf, dim3(fill_grid), dim3(256), 0, stream, scores, total) !=
+        cudaSuccess)
+        return HSS_ERR_CUDA;
+    if (launch_pdl(score_tc_kernel, dim3(grid), dim3(kThreads), L.total_bytes, stream, tmap_a,
+                   tmap_q, p) != cudaSuccess)
+        return HSS_ERR_CUDA;
+    return HSS_OK;
 }
 
 }  // namespace hss
