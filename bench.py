@@ -46,6 +46,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true",
                    help="launch every call from the host instead of replaying a CUDA graph")
+    p.add_argument("--unfused", action="store_true",
+                   help="decode: four separate calls per layer instead of hss_layer_step")
     return p.parse_args(argv)
 
 
@@ -206,11 +208,12 @@ class DecodeWorkload(_Base):
 
     name = "decode"
 
-    def __init__(self, device, seed: int):
+    def __init__(self, device, seed: int, unfused: bool = False):
         super().__init__(device)
         import workloads as W
 
         torch, hss = self.torch, self.hss
+        self.unfused = unfused
         self.case = c = W.decode(seed=seed, device=device)
         self.dims = d = c.dims
         self.L = d.num_layers
@@ -232,16 +235,24 @@ class DecodeWorkload(_Base):
                               device=device)
         self.scores = torch.empty(self.L, self.n, dtype=torch.float32, device=device)
         self.victims = torch.empty(self.L, 1, self.k, dtype=torch.int32, device=device)
+        self.ws_bytes = hss.hss_layer_step_workspace_bytes(1)
+        self.ws = torch.zeros(self.ws_bytes // 4, dtype=torch.int32, device=device)
         torch.cuda.synchronize()
 
     units_per_step = property(lambda self: self.L * self.n)
-    launches_per_step = property(lambda self: self.L * 4)
+    launches_per_step = property(lambda self: self.L * (4 if self.unfused else 2))
 
     def layer_call(self, l: int, K_new=None, Q=None):
         hss, d = self.hss, self.dims
-        hss.hss_project_kv_blocks(d, self.P, self.K_new[l] if K_new is None else K_new, l,
-                                  self.new_ids, 1, self.A)
-        hss.hss_project_q(d, self.P, self.Q[l] if Q is None else Q, 1, self.Qp[l])
+        K_new = self.K_new[l] if K_new is None else K_new
+        Q = self.Q[l] if Q is None else Q
+        if not self.unfused:
+            hss.hss_layer_step(d, self.P, K_new, self.new_ids, 1, Q, 1, self.Qp[l], self.A, l,
+                               self.table, self.offs, 1, self.n, self.scores[l], self.k,
+                               self.victims[l], self.ws, self.ws_bytes)
+            return
+        hss.hss_project_kv_blocks(d, self.P, K_new, l, self.new_ids, 1, self.A)
+        hss.hss_project_q(d, self.P, Q, 1, self.Qp[l])
         hss.hss_score_blocks(d, self.Qp[l], 1, self.A, l, self.table, self.offs, 1, self.n,
                              self.scores[l])
         hss.hss_rank_victims(self.scores[l], self.offs, 1, self.n, self.k, self.victims[l])
@@ -267,7 +278,8 @@ class DecodeWorkload(_Base):
                 f"{d.num_kv_heads} kv heads, head_dim {d.head_dim}, r {d.r}, block_size "
                 f"{d.block_size}, 1 sequence of {self.n * d.block_size} tokens ({self.n} blocks, "
                 f"permuted table), 1 query row, bottom-{self.k}; per layer call: project the "
-                f"block being written, project Q, score, rank")
+                f"block being written, project Q, score, rank"
+                + (" (four calls)" if self.unfused else " (hss_layer_step: 2 launches)"))
 
     l2_note = ("no flush: each step reads 32 x 16 MiB = 512 MiB of A_g, above the 129 MB L2, "
                "so every layer call reads cold A_g")
@@ -700,7 +712,10 @@ def run_hss(args):
     __graft_entry__.build()
     import kv_cache_block_lowrank_gb300 as hss
 
-    wl = WORKLOADS[args.workload](device, args.seed + rank)
+    if args.workload == "decode":
+        wl = DecodeWorkload(device, args.seed + rank, unfused=args.unfused)
+    else:
+        wl = WORKLOADS[args.workload](device, args.seed + rank)
     peaks = measured_peaks()
     stream = torch.cuda.Stream(device=device)
     torch.cuda.synchronize()

@@ -180,6 +180,39 @@ hss_status hss_rank_victims(const float* scores, const int32_t* seq_offsets, int
                             int64_t total_blocks, int32_t k, int32_t* victims, void* stream);
 
 /*
+ * One predictor layer call in as few launches as the shape allows: project the newly
+ * written blocks into A_g and the query rows into Qp (one launch), score every table
+ * entry, and rank the victims of every sequence.  Results are the same as
+ *   hss_project_kv_blocks(K_new, new_ids) ; hss_project_q(Q) ; hss_score_blocks(path AUTO) ;
+ *   hss_rank_victims
+ * on the same stream (the same kernels compute them).  In the decode regime the victim
+ * ranking runs inside the scoring kernel: the last CTA to finish a sequence ranks it.
+ * This is the fused decode call the predictor page's per-step usage implies (module docs
+ * of "metrale_storage/predictor.rs": scores only rank eviction victims).
+ *
+ *   K_new, new_ids, num_new  blocks written this step (num_new may be 0), as in
+ *                            hss_project_kv_blocks
+ *   Q                        device, [num_seqs, rows_per_seq, num_q_heads, head_dim] bf16
+ *   Qp                       device, [num_seqs, rows_per_seq, num_q_heads, r] bf16 (output)
+ *   scores, victims          outputs, as in hss_score_blocks / hss_rank_victims
+ *   workspace                device, >= hss_layer_step_workspace_bytes(num_seqs) bytes,
+ *                            4-byte aligned: per-sequence completion counters.  Zero it once
+ *                            (e.g. cudaMemsetAsync) before its first use; every call leaves
+ *                            it zero again.  Two calls that share a workspace must not run
+ *                            at the same time on the GPU.
+ * Errors as in the four calls above; HSS_ERR_WORKSPACE_TOO_SMALL if the workspace is short.
+ */
+size_t hss_layer_step_workspace_bytes(int32_t num_seqs);
+
+hss_status hss_layer_step(const hss_dims* dims, const uint16_t* P, const uint16_t* K_new,
+                          const int32_t* new_ids, int64_t num_new, const uint16_t* Q,
+                          int32_t rows_per_seq, uint16_t* Qp, uint16_t* A_g, int32_t layer,
+                          const int32_t* block_table, const int32_t* seq_offsets,
+                          int32_t num_seqs, int64_t total_blocks, float* scores, int32_t k,
+                          int32_t* victims, void* workspace, size_t workspace_bytes,
+                          int32_t* dev_status, void* stream);
+
+/*
  * Device-side error word of the current device: the first HSS_ERR_* code a
  * kernel raised since the last read (HSS_ERR_DEVICE_TIMEOUT when a pipeline
  * wait ran out), or HSS_OK.  Synchronises `stream`, copies the word to

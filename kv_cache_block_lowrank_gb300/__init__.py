@@ -39,6 +39,7 @@ HSS_MAX_VICTIMS = 8192
 EXPORTED = (
     "hss_status_string", "hss_version", "hss_validate_dims", "hss_a_g_bytes", "hss_project_q",
     "hss_project_kv_blocks", "hss_score_blocks", "hss_rank_victims", "hss_read_device_error",
+    "hss_layer_step", "hss_layer_step_workspace_bytes",
 )
 
 
@@ -103,6 +104,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.hss_rank_victims.argtypes = [vp, vp, i32, i64, i32, vp, vp]
     lib.hss_read_device_error.restype = i32
     lib.hss_read_device_error.argtypes = [ctypes.POINTER(i32), vp]
+    lib.hss_layer_step_workspace_bytes.restype = sz
+    lib.hss_layer_step_workspace_bytes.argtypes = [i32]
+    lib.hss_layer_step.restype = i32
+    lib.hss_layer_step.argtypes = [dp, vp, vp, vp, i64, vp, i32, vp, vp, i32, vp, vp, i32, i64,
+                                   vp, i32, vp, vp, sz, vp, vp]
     _lib = lib
     return lib
 
@@ -183,6 +189,24 @@ def hss_rank_victims(scores, seq_offsets, num_seqs: int, total_blocks: int, k: i
     st = load().hss_rank_victims(_ptr(scores), _ptr(seq_offsets), int(num_seqs),
                                  int(total_blocks), int(k), _ptr(victims), _stream(stream))
     _check(st, "hss_rank_victims")
+
+
+def hss_layer_step_workspace_bytes(num_seqs: int) -> int:
+    return load().hss_layer_step_workspace_bytes(int(num_seqs))
+
+
+def hss_layer_step(dims, P, K_new, new_ids, num_new: int, Q, rows_per_seq: int, Qp, A_g,
+                   layer: int, block_table, seq_offsets, num_seqs: int, total_blocks: int,
+                   scores, k: int, victims, workspace, workspace_bytes: int, dev_status=None,
+                   stream=None) -> None:
+    """One layer call: project new blocks and queries, score, rank (fused where possible)."""
+    st = load().hss_layer_step(ctypes.byref(hss_dims.of(dims)), _ptr(P), _ptr(K_new),
+                               _ptr(new_ids), int(num_new), _ptr(Q), int(rows_per_seq), _ptr(Qp),
+                               _ptr(A_g), int(layer), _ptr(block_table), _ptr(seq_offsets),
+                               int(num_seqs), int(total_blocks), _ptr(scores), int(k),
+                               _ptr(victims), _ptr(workspace), int(workspace_bytes),
+                               _ptr(dev_status), _stream(stream))
+    _check(st, "hss_layer_step")
 
 
 def hss_read_device_error(stream=None) -> int:

@@ -200,6 +200,111 @@ hss_status hss_rank_victims(const float* scores, const int32_t* seq_offsets, int
                                static_cast<cudaStream_t>(stream));
 }
 
+size_t hss_layer_step_workspace_bytes(int32_t num_seqs) {
+    if (num_seqs <= 0) return 0;
+    const size_t b = static_cast<size_t>(num_seqs) * sizeof(int32_t);
+    return (b + 255) / 256 * 256;
+}
+
+hss_status hss_layer_step(const hss_dims* dims, const uint16_t* P, const uint16_t* K_new,
+                          const int32_t* new_ids, int64_t num_new, const uint16_t* Q,
+                          int32_t rows_per_seq, uint16_t* Qp, uint16_t* A_g, int32_t layer,
+                          const int32_t* block_table, const int32_t* seq_offsets,
+                          int32_t num_seqs, int64_t total_blocks, float* scores, int32_t k,
+                          int32_t* victims, void* workspace, size_t workspace_bytes,
+                          int32_t* dev_status, void* stream) {
+    hss_status st = check_dims(dims);
+    if (st != HSS_OK) return st;
+    if (layer < 0 || layer >= dims->num_layers) return HSS_ERR_OUT_OF_RANGE;
+    if (num_new < 0 || num_seqs < 0 || total_blocks < 0 || rows_per_seq < 1 ||
+        total_blocks > 0x7FFFFFFF || k < 1 || k > HSS_MAX_VICTIMS)
+        return HSS_ERR_INVALID_ARGUMENT;
+    if (num_seqs == 0 && total_blocks != 0) return HSS_ERR_INVALID_ARGUMENT;
+    if (P == nullptr || A_g == nullptr) return HSS_ERR_NULL_POINTER;
+    if (num_new > 0 && (K_new == nullptr || new_ids == nullptr)) return HSS_ERR_NULL_POINTER;
+    if (num_seqs > 0 && (Q == nullptr || Qp == nullptr || seq_offsets == nullptr ||
+                         victims == nullptr))
+        return HSS_ERR_NULL_POINTER;
+    if (total_blocks > 0 && (block_table == nullptr || scores == nullptr))
+        return HSS_ERR_NULL_POINTER;
+    if (!aligned16(P) || !aligned16(A_g) || (K_new != nullptr && !aligned16(K_new)) ||
+        (Q != nullptr && !aligned16(Q)) || (Qp != nullptr && !aligned16(Qp)))
+        return HSS_ERR_MISALIGNED;
+    if (num_seqs > 0) {
+        if (workspace == nullptr) return HSS_ERR_NULL_POINTER;
+        if (workspace_bytes < hss_layer_step_workspace_bytes(num_seqs))
+            return HSS_ERR_WORKSPACE_TOO_SMALL;
+        if ((reinterpret_cast<uintptr_t>(workspace) & 3u) != 0) return HSS_ERR_MISALIGNED;
+    }
+    const int64_t rows_per_block = static_cast<int64_t>(dims->block_size) * dims->num_kv_heads;
+    if (num_new > (int64_t{1} << 31) / rows_per_block) return HSS_ERR_INVALID_ARGUMENT;
+    if (static_cast<int64_t>(num_seqs) * rows_per_seq > (int64_t{1} << 40) / dims->num_q_heads)
+        return HSS_ERR_INVALID_ARGUMENT;
+
+    // Decide the scoring path before launching anything, so an unsupported shape enqueues
+    // nothing.
+    ScoreArgs a{};
+    a.Qp = Qp;
+    a.rows_per_seq = rows_per_seq;
+    a.A_g = A_g;
+    a.layer_offset_slots = static_cast<int64_t>(layer) * dims->max_blocks;
+    a.max_blocks = dims->max_blocks;
+    a.table = block_table;
+    a.seq_offsets = seq_offsets;
+    a.num_seqs = num_seqs;
+    a.total = total_blocks;
+    a.scores = scores;
+    a.num_q_heads = dims->num_q_heads;
+    a.num_kv_heads = dims->num_kv_heads;
+    a.r = dims->r;
+    a.block_size = dims->block_size;
+    a.dev_status = dev_status;
+    const int64_t nvec =
+        static_cast<int64_t>(rows_per_seq) * (dims->num_q_heads / dims->num_kv_heads);
+    const bool decode = nvec <= 16 && score_decode_supported(a);
+    if (total_blocks > 0 && !decode && !score_tc_supported(a)) return HSS_ERR_UNSUPPORTED_SHAPE;
+
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // 1. one launch projects the query rows and the newly written blocks
+    ProjectArgs q{};
+    q.P = P;
+    q.X = Q;
+    q.num_rows = static_cast<int64_t>(num_seqs) * rows_per_seq * dims->num_q_heads;
+    q.head_dim = dims->head_dim;
+    q.r = dims->r;
+    q.out = Qp;
+    q.block_ids = nullptr;
+    ProjectArgs kv{};
+    kv.P = P;
+    kv.X = K_new;
+    kv.num_rows = num_new * rows_per_block;
+    kv.head_dim = dims->head_dim;
+    kv.r = dims->r;
+    kv.out = A_g;
+    kv.block_ids = new_ids;
+    kv.num_kv_heads = dims->num_kv_heads;
+    kv.block_size = dims->block_size;
+    kv.max_blocks = dims->max_blocks;
+    kv.layer = layer;
+    kv.dev_status = dev_status;
+    st = launch_project2(q, &kv, s);
+    if (st != HSS_OK || num_seqs == 0) return st;
+    // 2. scores, with the ranking fused into the decode scorer where it fits
+    bool fused = false;
+    if (total_blocks > 0) {
+        if (decode) {
+            FusedRank fr{static_cast<int32_t*>(workspace), victims, k};
+            st = launch_score_decode(a, s, &fr, &fused);
+        } else {
+            st = launch_score_tc(a, s);
+        }
+        if (st != HSS_OK) return st;
+    }
+    // 3. otherwise a separate ranking launch
+    if (!fused) return launch_rank_victims(scores, seq_offsets, num_seqs, total_blocks, k, victims, s);
+    return HSS_OK;
+}
+
 hss_status hss_read_device_error(int32_t* status, void* stream) {
     if (status == nullptr) return HSS_ERR_NULL_POINTER;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);

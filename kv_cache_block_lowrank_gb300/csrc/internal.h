@@ -64,6 +64,8 @@ struct ProjectArgs {
     int32_t* dev_status;
 };
 hss_status launch_project(const ProjectArgs& a, cudaStream_t stream);
+// Both segments in one launch (a1 may be nullptr or empty); they must share head_dim and r.
+hss_status launch_project2(const ProjectArgs& a0, const ProjectArgs* a1, cudaStream_t stream);
 bool project_shape_supported(int32_t head_dim, int32_t r);
 
 // ------------------------------------------------------------------- decode scorer
@@ -84,7 +86,17 @@ struct ScoreArgs {
     int32_t block_size;
     int32_t* dev_status;
 };
-hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream);
+// Victim ranking fused into the decode scorer: counters are the caller's per-sequence
+// completion counters (zero on entry, left zero on exit).
+struct FusedRank {
+    int32_t* counters;
+    int32_t* victims;
+    int32_t k;
+};
+// With fr != nullptr the ranking is fused when the shape allows; *fused reports whether it
+// was (otherwise the caller must rank separately).
+hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream,
+                               const FusedRank* fr = nullptr, bool* fused = nullptr);
 bool score_decode_supported(const ScoreArgs& a);
 hss_status launch_score_tc(const ScoreArgs& a, cudaStream_t stream);
 bool score_tc_supported(const ScoreArgs& a);

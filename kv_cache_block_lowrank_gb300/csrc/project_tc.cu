@@ -60,13 +60,20 @@ __host__ __device__ inline ProjLayout make_layout(int head_dim, int r, int smem_
     return L;
 }
 
+// One launch projects up to two row segments (e.g. the query rows and the newly written
+// key blocks of a decode step), each with its own input map and output mapping.
+struct ProjSegment {
+    int64_t num_rows;
+    int64_t tiles;             // ceil(num_rows / 128)
+    uint16_t* out;
+    const int32_t* block_ids;  // nullptr: rows go to out + m * r (Qp); else A_g slot rows
+};
+
 struct ProjParams {
     const uint16_t* P;
-    int64_t num_rows;
     int32_t head_dim;
     int32_t r;
-    uint16_t* out;
-    const int32_t* block_ids;  // nullptr: Qp mode
+    ProjSegment seg[2];
     int32_t num_kv_heads;
     int32_t block_size;
     int64_t max_blocks;
@@ -76,7 +83,9 @@ struct ProjParams {
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
-    project_kernel(const __grid_constant__ CUtensorMap tmap_x, const ProjParams p, const int stages) {
+    project_kernel(const __grid_constant__ CUtensorMap tmap_x0,
+                   const __grid_constant__ CUtensorMap tmap_x1, const ProjParams p,
+                   const int stages) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -96,7 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int r = p.r;
-    const int64_t num_tiles = (p.num_rows + kBM - 1) / kBM;
+    const int64_t num_tiles = p.seg[0].tiles + p.seg[1].tiles;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -155,7 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            tma_prefetch_desc(&tmap_x);
+            tma_prefetch_desc(&tmap_x0);
+            if (p.seg[1].tiles > 0) tma_prefetch_desc(&tmap_x1);
             int stage = 0;
             uint32_t phase = 0;
             int64_t issued = 0;
@@ -167,9 +177,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(stage_bytes));
                 uint8_t* dst = sA + stage * stage_bytes;
+                const bool second = tile >= p.seg[0].tiles;
+                const CUtensorMap* map = second ? &tmap_x1 : &tmap_x0;
+                const int64_t local = second ? tile - p.seg[0].tiles : tile;
                 for (int c = 0; c < kchunks; ++c) {
-                    tma_load_2d(dst + c * kChunkBytes, &tmap_x, &full[stage], c * kChunkElems,
-                                static_cast<int32_t>(tile * kBM));
+                    tma_load_2d(dst + c * kChunkBytes, map, &full[stage], c * kChunkElems,
+                                static_cast<int32_t>(local * kBM));
                 }
                 ++issued;
                 if (++stage == stages) {
@@ -238,19 +251,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after_sync();
-            const int64_t m = tile * kBM + row_in_tile;
+            const bool second = tile >= p.seg[0].tiles;
+            const ProjSegment& sg = second ? p.seg[1] : p.seg[0];
+            const int64_t m = (second ? tile - p.seg[0].tiles : tile) * kBM + row_in_tile;
             uint16_t* dst = nullptr;
-            if (m < p.num_rows) {
-                if (p.block_ids == nullptr) {
-                    dst = p.out + m * r;
+            if (m < sg.num_rows) {
+                if (sg.block_ids == nullptr) {
+                    dst = sg.out + m * r;
                 } else {
                     const int64_t i = m / rows_per_block;
                     const int rem = static_cast<int>(m - i * rows_per_block);
                     const int t = rem / p.num_kv_heads;
                     const int h = rem - t * p.num_kv_heads;
-                    const int64_t id = p.block_ids[i];
+                    const int64_t id = sg.block_ids[i];
                     if (id >= 0 && id < p.max_blocks) {
-                        dst = p.out + (((p.layer_slots + id) * p.num_kv_heads + h) * p.block_size +
+                        dst = sg.out + (((p.layer_slots + id) * p.num_kv_heads + h) * p.block_size +
                                        t) * static_cast<int64_t>(r);
                     } else if (rem == 0) {
                         raise_error(p.dev_status, p.lib_error, HSS_ERR_OUT_OF_RANGE);
@@ -325,27 +340,38 @@ bool project_shape_supported(int32_t head_dim, int32_t r) {
     return L.stages >= 2;
 }
 
-hss_status launch_project(const ProjectArgs& a, cudaStream_t stream) {
-    if (a.num_rows == 0) return HSS_OK;
+static bool encode_rows_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map,
+                            const uint16_t* X, int64_t rows, int32_t head_dim) {
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(head_dim) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kChunkElems), static_cast<cuuint32_t>(kBM)};
+    const cuuint32_t estride[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(X), gdim, gstride,
+               box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+hss_status launch_project2(const ProjectArgs& a0, const ProjectArgs* a1, cudaStream_t stream) {
+    const int64_t rows0 = a0.num_rows, rows1 = a1 != nullptr ? a1->num_rows : 0;
+    if (rows0 == 0 && rows1 == 0) return HSS_OK;
     const DeviceInfo* dev = current_device_info();
     if (dev == nullptr) return HSS_ERR_CUDA;
-    if (!project_shape_supported(a.head_dim, a.r)) return HSS_ERR_UNSUPPORTED_SHAPE;
-    const ProjLayout L = make_layout(a.head_dim, a.r, dev->max_smem_optin);
+    if (!project_shape_supported(a0.head_dim, a0.r)) return HSS_ERR_UNSUPPORTED_SHAPE;
+    const ProjLayout L = make_layout(a0.head_dim, a0.r, dev->max_smem_optin);
     if (L.stages < 2) return HSS_ERR_UNSUPPORTED_SHAPE;
     auto enc = encoder();
     if (enc == nullptr) return HSS_ERR_CUDA;
 
-    CUtensorMap tmap;
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(a.head_dim),
-                                static_cast<cuuint64_t>(a.num_rows)};
-    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(a.head_dim) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kChunkElems), static_cast<cuuint32_t>(kBM)};
-    const cuuint32_t estride[2] = {1, 1};
-    if (enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a.X), gdim, gstride,
-            box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
-        return HSS_ERR_CUDA;
+    // Segment 0 is the first non-empty one.
+    const ProjectArgs* s0 = rows0 > 0 ? &a0 : a1;
+    const ProjectArgs* s1 = rows0 > 0 && rows1 > 0 ? a1 : nullptr;
+    CUtensorMap map0, map1;
+    if (!encode_rows_map(enc, &map0, s0->X, s0->num_rows, a0.head_dim)) return HSS_ERR_CUDA;
+    if (s1 != nullptr) {
+        if (!encode_rows_map(enc, &map1, s1->X, s1->num_rows, a0.head_dim)) return HSS_ERR_CUDA;
+    } else {
+        map1 = map0;
     }
     {
         std::lock_guard<std::mutex> lk(g_smem_mu);
@@ -359,25 +385,39 @@ hss_status launch_project(const ProjectArgs& a, cudaStream_t stream) {
         }
     }
     ProjParams p;
-    p.P = a.P;
-    p.num_rows = a.num_rows;
-    p.head_dim = a.head_dim;
-    p.r = a.r;
-    p.out = a.out;
-    p.block_ids = a.block_ids;
-    p.num_kv_heads = a.num_kv_heads;
-    p.block_size = a.block_size;
-    p.max_blocks = a.max_blocks;
-    p.layer_slots = static_cast<int64_t>(a.layer) * a.max_blocks;
-    p.dev_status = a.dev_status;
+    p.P = a0.P;
+    p.head_dim = a0.head_dim;
+    p.r = a0.r;
+    const ProjectArgs* segs[2] = {s0, s1};
+    const ProjectArgs* kv = nullptr;
+    for (int i = 0; i < 2; ++i) {
+        if (segs[i] == nullptr) {
+            p.seg[i] = ProjSegment{0, 0, nullptr, nullptr};
+            continue;
+        }
+        p.seg[i].num_rows = segs[i]->num_rows;
+        p.seg[i].tiles = (segs[i]->num_rows + kBM - 1) / kBM;
+        p.seg[i].out = segs[i]->out;
+        p.seg[i].block_ids = segs[i]->block_ids;
+        if (segs[i]->block_ids != nullptr) kv = segs[i];
+    }
+    p.num_kv_heads = kv != nullptr ? kv->num_kv_heads : 1;
+    p.block_size = kv != nullptr ? kv->block_size : 1;
+    p.max_blocks = kv != nullptr ? kv->max_blocks : 0;
+    p.layer_slots = kv != nullptr ? static_cast<int64_t>(kv->layer) * kv->max_blocks : 0;
+    p.dev_status = kv != nullptr ? kv->dev_status : nullptr;
     p.lib_error = dev->error_word;
-    const int64_t num_tiles = (a.num_rows + kBM - 1) / kBM;
+    const int64_t num_tiles = p.seg[0].tiles + p.seg[1].tiles;
     const int grid = static_cast<int>(std::min<int64_t>(num_tiles, dev->num_sms));
     const int stages = L.stages;
-    if (launch_pdl(project_kernel, dim3(grid), dim3(kThreads), L.total_bytes, stream, tmap, p,
-                   stages) != cudaSuccess)
+    if (launch_pdl(project_kernel, dim3(grid), dim3(kThreads), L.total_bytes, stream, map0, map1,
+                   p, stages) != cudaSuccess)
         return HSS_ERR_CUDA;
     return HSS_OK;
+}
+
+hss_status launch_project(const ProjectArgs& a, cudaStream_t stream) {
+    return launch_project2(a, nullptr, stream);
 }
 
 }  // namespace hss

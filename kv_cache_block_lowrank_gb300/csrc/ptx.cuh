@@ -238,6 +238,13 @@ __host__ __device__ __forceinline__ uint32_t swizzled_offset(uint32_t row, uint3
     return lin ^ (((lin >> 7) & mask) << 4);
 }
 
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 family).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // ---------------------------------------------------------------------------------------------
 // bf16 helpers
 // ---------------------------------------------------------------------------------------------

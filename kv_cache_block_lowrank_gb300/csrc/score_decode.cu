@@ -23,7 +23,7 @@
 #include <algorithm>
 #include <cmath>
 
-#include "ptx.cuh"
+#include "rank_device.cuh"
 
 namespace hss {
 namespace {
@@ -51,6 +51,16 @@ struct DecodeParams {
     int32_t bs;
     int32_t g;
     int32_t nvec;  // rows * g query vectors per kv head
+    // Fused victim ranking (counters == nullptr: off).  counters[s] counts the entries of
+    // sequence s scored so far; the CTA that completes a sequence ranks it and resets the
+    // counter to zero.
+    int32_t* counters;
+    int32_t* victims;
+    int32_t k;
+    int32_t sel_cap;
+    int32_t keys_cap;
+    int32_t frag_bytes_cta;  // offset of the ranking scratch in shared memory
+    int32_t todo_cap;        // sequences one CTA can complete: its entry count
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
@@ -76,7 +86,8 @@ __device__ __forceinline__ int frag_r_offset(int ks, int t) {
 
 template <int KSTEPS, int NT>
 __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const DecodeParams p) {
-    extern __shared__ uint2 frag_cache_all[];
+    extern __shared__ __align__(16) uint8_t smem_dec[];
+    uint2* frag_cache_all = reinterpret_cast<uint2*>(smem_dec);
     constexpr int kLoadsPerRow = KSTEPS == 1 ? 1 : KSTEPS / 2;  // 16-byte (or 8-byte) loads
     constexpr int kRegsPerTile = KSTEPS == 1 ? 4 : 4 * KSTEPS;  // both row halves
     constexpr int kTilesPerBatch = 64 / kRegsPerTile;
@@ -92,7 +103,7 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
     const int64_t i_begin = wid * p.entries_per_warp;
     grid_dependency_wait();
     grid_launch_dependents();
-    if (i_begin >= p.total) return;
+    if (i_begin < p.total) {
     const int64_t i_end = min(p.total, i_begin + p.entries_per_warp);
 
     // Sequence of the first entry: the last s with seq_offsets[s] <= i_begin.
@@ -237,6 +248,60 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
             if (lane == 0) p.scores[i] = best;
         }
     }
+    }  // i_begin < total
+    if (p.counters == nullptr) return;
+
+    // ---- fused ranking: the CTA that completes a sequence ranks it
+    constexpr int kThreadsFused = kWarpsMax * 32;
+    uint8_t* rank_smem = smem_dec + p.frag_bytes_cta;
+    uint64_t* sel = reinterpret_cast<uint64_t*>(rank_smem);
+    rankdev::RankShared* sh = reinterpret_cast<rankdev::RankShared*>(sel + p.sel_cap);
+    uint32_t* keys = reinterpret_cast<uint32_t*>(sh + 1);
+    int* todo = reinterpret_cast<int*>(keys + p.keys_cap);  // [todo_cap + 1]
+    if (lane == 0) __threadfence();  // this warp's scores before the CTA's count
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int ntodo = 0;
+        const int64_t per_cta = p.entries_per_warp * (blockDim.x >> 5);
+        const int64_t cb = static_cast<int64_t>(blockIdx.x) * per_cta;
+        const int64_t ce = min(p.total, cb + per_cta);
+        if (cb < ce) {
+            int lo2 = 0, hi2 = p.num_seqs;  // last s with seq_offsets[s] <= cb
+            while (hi2 - lo2 > 1) {
+                const int mid = (lo2 + hi2) >> 1;
+                if (static_cast<int64_t>(__ldg(&p.seq_offsets[mid])) <= cb) lo2 = mid; else hi2 = mid;
+            }
+            for (int q = lo2; q < p.num_seqs; ++q) {
+                const int64_t a = __ldg(&p.seq_offsets[q]), b = __ldg(&p.seq_offsets[q + 1]);
+                if (a >= ce) break;
+                const int64_t cnt = min(ce, b) - max(cb, a);
+                if (cnt <= 0) continue;
+                const int old = atomicAdd(&p.counters[q], static_cast<int>(cnt));
+                if (old + cnt == b - a && ntodo < p.todo_cap) todo[1 + ntodo++] = q;
+            }
+        }
+        todo[0] = ntodo;
+    }
+    __syncthreads();
+    const int ntodo = todo[0];
+    if (ntodo > 0) __threadfence();  // every other CTA's scores of these sequences are visible
+    for (int t = 0; t < ntodo; ++t) {
+        const int q = todo[1 + t];
+        const int64_t a = __ldg(&p.seq_offsets[q]);
+        const int n = static_cast<int>(__ldg(&p.seq_offsets[q + 1]) - a);
+        rankdev::rank_sequence<kThreadsFused>(p.scores + a, n, p.k,
+                                              p.victims + static_cast<int64_t>(q) * p.k, sel,
+                                              p.sel_cap, sh, keys, p.keys_cap);
+        if (threadIdx.x == 0) p.counters[q] = 0;  // ready for the next call
+    }
+    // Empty sequences have no entries to complete them: CTA 0 writes their -1 rows.
+    if (blockIdx.x == 0) {
+        for (int q = threadIdx.x; q < p.num_seqs; q += blockDim.x) {
+            if (__ldg(&p.seq_offsets[q + 1]) == __ldg(&p.seq_offsets[q])) {
+                for (int j = 0; j < p.k; ++j) p.victims[static_cast<int64_t>(q) * p.k + j] = -1;
+            }
+        }
+    }
 }
 
 template <int KSTEPS, int NT>
@@ -271,7 +336,9 @@ bool score_decode_supported(const ScoreArgs& a) {
     return frag_bytes_per_warp(a) <= kFragBudgetBytes;
 }
 
-hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream) {
+hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream, const FusedRank* fr,
+                               bool* fused) {
+    if (fused != nullptr) *fused = false;
     if (a.total == 0) return HSS_OK;
     const DeviceInfo* dev = current_device_info();
     if (dev == nullptr) return HSS_ERR_CUDA;
@@ -295,15 +362,40 @@ hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream) {
     p.bs = a.block_size;
     p.g = a.num_q_heads / a.num_kv_heads;
     p.nvec = a.rows_per_seq * p.g;
+    p.counters = nullptr;
+    p.victims = nullptr;
+    p.k = 0;
+    p.sel_cap = 0;
+    p.keys_cap = 0;
+    p.todo_cap = 0;
 
     const int fb = frag_bytes_per_warp(a);
     const int warps_per_cta = std::max(1, std::min(kWarpsMax, kFragBudgetBytes / fb));
-    const int smem = warps_per_cta * fb;
+    int smem = warps_per_cta * fb;
+    p.frag_bytes_cta = smem;
     // Enough warps for two CTAs per SM; each warp takes a contiguous run of entries.
     const int64_t target_warps = static_cast<int64_t>(dev->num_sms) * 2 * warps_per_cta;
     p.entries_per_warp = std::max<int64_t>(1, (a.total + target_warps - 1) / target_warps);
     const int64_t warps = (a.total + p.entries_per_warp - 1) / p.entries_per_warp;
     const int grid = static_cast<int>((warps + warps_per_cta - 1) / warps_per_cta);
+    // The ranking can ride along when a whole CTA of 8 warps is there to run it, every
+    // sequence's keys fit in shared memory and the extra shared memory stays modest.
+    if (fr != nullptr && warps_per_cta == kWarpsMax && a.total <= rankdev::kKeysCap) {
+        const int sel_cap = rankdev::rank_sel_cap(fr->k);
+        const int keys_cap = static_cast<int>(a.total);
+        const int todo_cap = static_cast<int>(p.entries_per_warp * warps_per_cta);
+        const int extra = rankdev::rank_smem_bytes(sel_cap, keys_cap) + (todo_cap + 1) * 4;
+        if (smem + extra <= 100 * 1024) {
+            p.todo_cap = todo_cap;
+            p.counters = fr->counters;
+            p.victims = fr->victims;
+            p.k = fr->k;
+            p.sel_cap = sel_cap;
+            p.keys_cap = keys_cap;
+            smem += extra;
+            if (fused != nullptr) *fused = true;
+        }
+    }
 
     const int ksteps = a.r / 16;
     const int nt = (p.nvec + 7) / 8;

@@ -18,7 +18,9 @@
 // when its run crosses into the next (s, c, slice).  Roles (persistent, 1 CTA per SM):
 //   warp 0      TMA producer (Qp slices; per-block A_g boxes into a ring of stages)
 //   warp 1      TMEM allocator (512 columns) and MMA issuer, M=128, N=256, K=16 steps
-//   warps 2..5  epilogue: tcgen05.ld, running max per token, block max, float atomic max
+//   warps 2..9  epilogue, two warpgroups: warpgroup e drains accumulator buffer e, so one
+//               drains while the MMA fills the other; tcgen05.ld four 32-column loads per
+//               wait, 3-input max, block max by shuffles, one float atomic max per block
 // Scores are first set to -inf (separate tiny kernel); every unit atomically maxes its
 // partial block maximum into the block's score.
 #include <cudaTypedefs.h>
@@ -34,7 +36,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer warp, MMA warp, two epilogue warpgroups
 constexpr int kTileTokens = 128;     // UMMA M
 constexpr int kNChunk = 256;         // UMMA N per accumulator buffer
 constexpr int kMaxSliceVecs = 1024;  // query vectors resident per slice
@@ -325,42 +327,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // Epilogue: warp w owns TMEM lanes 32 * (w % 4) .. + 31 = token rows of the tile.
+        // Epilogue: warpgroup eg drains accumulator buffer eg (every other N chunk); warp w
+        // owns TMEM lanes 32 * (w % 4) .. + 31 = token rows of the tile.
+        const int eg = (warp - 2) >> 2;
         const int quarter = warp & 3;
         const int token = quarter * 32 + lane;
-        int64_t it = 0;
+        int64_t it = 0;  // global chunk counter, shared numbering with the MMA warp
         bool ok = true;
         for (int64_t u = u_begin; u < u_end && ok; ++u) {
             const Unit x = decode_unit(u, p, units_before);
             float run = -INFINITY;
+            bool any = false;
             for (int nc = 0; nc < nchunks; ++nc, ++it) {
-                const int acc = static_cast<int>(it & 1);
+                if (static_cast<int>(it & 1) != eg) continue;
+                const int acc = eg;
                 const bool got = mbar_wait(&t_full[acc], static_cast<uint32_t>((it >> 1) & 1));
                 if (__any_sync(0xffffffffu, !got) || *(volatile int*)abort_flag) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
+                any = true;
                 const int v0 = x.q * p.slice + nc * kNChunk;  // first query vector of the chunk
                 const int valid = min(kNChunk, p.nvec - v0);
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        static_cast<uint32_t>(acc * kNChunk);
-                for (int c0 = 0; c0 < kNChunk; c0 += 32) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(taddr + c0, v);
+                for (int half = 0; half < kNChunk; half += 128) {
+                    uint32_t v[128];
+                    tmem_ld_32x32b_x32(taddr + half, v);
+                    tmem_ld_32x32b_x32(taddr + half + 32, v + 32);
+                    tmem_ld_32x32b_x32(taddr + half + 64, v + 64);
+                    tmem_ld_32x32b_x32(taddr + half + 96, v + 96);
                     tmem_ld_wait();
-                    if (c0 + 32 <= valid) {
-                        float m0 = __uint_as_float(v[0]), m1 = __uint_as_float(v[1]);
+                    if (half + 128 <= valid) {
+                        float m0 = run, m1 = run, m2 = run, m3 = run;
 #pragma unroll
-                        for (int j = 2; j < 32; j += 2) {
-                            m0 = fmaxf(m0, __uint_as_float(v[j]));
-                            m1 = fmaxf(m1, __uint_as_float(v[j + 1]));
+                        for (int j = 0; j < 128; j += 8) {
+                            m0 = fmax3(m0, __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+                            m1 = fmax3(m1, __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+                            m2 = fmax3(m2, __uint_as_float(v[j + 4]), __uint_as_float(v[j + 5]));
+                            m3 = fmax3(m3, __uint_as_float(v[j + 6]), __uint_as_float(v[j + 7]));
                         }
-                        run = fmaxf(run, fmaxf(m0, m1));
+                        run = fmax3(fmaxf(m0, m1), m2, m3);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (c0 + j < valid) run = fmaxf(run, __uint_as_float(v[j]));
+                        for (int j = 0; j < 128; ++j)
+                            if (half + j < valid) run = fmaxf(run, __uint_as_float(v[j]));
                     }
                 }
                 tc_fence_before_sync();
@@ -368,6 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&t_empty[acc]);
             }
             if (!ok) break;
+            if (!any) continue;  // no chunk of this unit landed in this warpgroup's buffer
             // Max over the block's tokens: block_size consecutive lanes.
             for (int off = p.bs >> 1; off > 0; off >>= 1)
                 run = fmaxf(run, __shfl_xor_sync(0xffffffffu, run, off));

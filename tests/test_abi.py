@@ -163,3 +163,19 @@ def _load_fresh(mod, path):
         return mod.load(path)
     finally:
         mod._lib = saved
+
+
+def test_layer_step_validation(lib):
+    assert hss.hss_layer_step_workspace_bytes(0) == 0
+    assert hss.hss_layer_step_workspace_bytes(1) == 256
+    assert hss.hss_layer_step_workspace_bytes(65) == 512
+    base = lambda **o: [o.get("d", dims()), FAKE, FAKE, FAKE, o.get("num_new", 1), FAKE, 1, FAKE,
+                        FAKE, o.get("layer", 0), FAKE, FAKE, o.get("S", 1), 10, FAKE,
+                        o.get("k", 4), FAKE, o.get("ws", FAKE), o.get("wsb", 256), None, 0]
+    assert status_of(hss.hss_layer_step, *base(wsb=16)) == hss.HSS_ERR_WORKSPACE_TOO_SMALL
+    assert status_of(hss.hss_layer_step, *base(ws=None)) == hss.HSS_ERR_NULL_POINTER
+    assert status_of(hss.hss_layer_step, *base(layer=99)) == hss.HSS_ERR_OUT_OF_RANGE
+    assert status_of(hss.hss_layer_step, *base(k=0)) == hss.HSS_ERR_INVALID_ARGUMENT
+    assert status_of(hss.hss_layer_step, *base(num_new=-1)) == hss.HSS_ERR_INVALID_ARGUMENT
+    assert status_of(hss.hss_layer_step, *base(d=dims(num_kv_heads=3))) == \
+        hss.HSS_ERR_INVALID_DIMS
