@@ -213,6 +213,38 @@ hss_status hss_layer_step(const hss_dims* dims, const uint16_t* P, const uint16_
                           int32_t* dev_status, void* stream);
 
 /*
+ * hss_layer_step for callers that cannot allocate device memory.  (The predictor pages have
+ * no counterpart: this is a calling convention of this library.)
+ *
+ * hss_layer_step needs a caller-allocated workspace.  Some callers cannot call cudaMalloc
+ * there: an engine whose memory arena owns the GPU's memory and allows no allocation after
+ * start-up, a library hosted by a process that hands it no allocator, or a caller that only
+ * holds raw pointers to its own buffers.  This variant takes no workspace: the completion
+ * counters live in a fixed array inside the library, HSS_LAYER_STEP_STATIC_MAX_SEQS int32
+ * words (16 KiB) on every GPU that loads it, kept until the process exits.  It allocates
+ * nothing and calls no allocating routine.
+ *
+ *   Arguments and results: as hss_layer_step, without workspace / workspace_bytes.
+ *   num_seqs > HSS_LAYER_STEP_STATIC_MAX_SEQS  -> HSS_ERR_WORKSPACE_TOO_SMALL, nothing enqueued.
+ *   Each call first clears the counters it uses (a memset on `stream`), then runs the same
+ *   kernels as hss_layer_step.
+ *   The first call on a device looks up the array's device address (cudaGetSymbolAddress);
+ *   make that first call before any stream capture on that device.
+ *   All calls share the one array: calls that overlap on the GPU (on different streams, or
+ *   unordered) race and give wrong victims.  Order them on one stream.
+ */
+#define HSS_LAYER_STEP_STATIC_MAX_SEQS 4096
+
+int32_t hss_layer_step_static_max_seqs(void);
+
+hss_status hss_layer_step_static(const hss_dims* dims, const uint16_t* P, const uint16_t* K_new,
+                                 const int32_t* new_ids, int64_t num_new, const uint16_t* Q,
+                                 int32_t rows_per_seq, uint16_t* Qp, uint16_t* A_g, int32_t layer,
+                                 const int32_t* block_table, const int32_t* seq_offsets,
+                                 int32_t num_seqs, int64_t total_blocks, float* scores, int32_t k,
+                                 int32_t* victims, int32_t* dev_status, void* stream);
+
+/*
  * Device-side error word of the current device: the first HSS_ERR_* code a
  * kernel raised since the last read (HSS_ERR_DEVICE_TIMEOUT when a pipeline
  * wait ran out), or HSS_OK.  Synchronises `stream`, copies the word to

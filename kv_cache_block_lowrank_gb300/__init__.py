@@ -39,7 +39,8 @@ HSS_MAX_VICTIMS = 8192
 EXPORTED = (
     "hss_status_string", "hss_version", "hss_validate_dims", "hss_a_g_bytes", "hss_project_q",
     "hss_project_kv_blocks", "hss_score_blocks", "hss_rank_victims", "hss_read_device_error",
-    "hss_layer_step", "hss_layer_step_workspace_bytes",
+    "hss_layer_step", "hss_layer_step_workspace_bytes", "hss_layer_step_static",
+    "hss_layer_step_static_max_seqs",
 )
 
 
@@ -106,6 +107,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.hss_read_device_error.argtypes = [ctypes.POINTER(i32), vp]
     lib.hss_layer_step_workspace_bytes.restype = sz
     lib.hss_layer_step_workspace_bytes.argtypes = [i32]
+    lib.hss_layer_step_static_max_seqs.restype = i32
+    lib.hss_layer_step_static_max_seqs.argtypes = []
+    lib.hss_layer_step_static.restype = i32
+    lib.hss_layer_step_static.argtypes = [dp, vp, vp, vp, i64, vp, i32, vp, vp, i32, vp, vp, i32,
+                                          i64, vp, i32, vp, vp, vp]
     lib.hss_layer_step.restype = i32
     lib.hss_layer_step.argtypes = [dp, vp, vp, vp, i64, vp, i32, vp, vp, i32, vp, vp, i32, i64,
                                    vp, i32, vp, vp, sz, vp, vp]
@@ -207,6 +213,29 @@ def hss_layer_step(dims, P, K_new, new_ids, num_new: int, Q, rows_per_seq: int, 
                                _ptr(victims), _ptr(workspace), int(workspace_bytes),
                                _ptr(dev_status), _stream(stream))
     _check(st, "hss_layer_step")
+
+
+def hss_layer_step_static_max_seqs() -> int:
+    return load().hss_layer_step_static_max_seqs()
+
+
+def hss_layer_step_static(dims, P, K_new, new_ids, num_new: int, Q, rows_per_seq: int, Qp, A_g,
+                          layer: int, block_table, seq_offsets, num_seqs: int, total_blocks: int,
+                          scores, k: int, victims, dev_status=None, stream=None) -> None:
+    """hss_layer_step without a workspace, for callers that cannot allocate device memory.
+
+    The completion counters live in a fixed array inside the library (at most
+    hss_layer_step_static_max_seqs() sequences per call).  Calls share that array, so they
+    must not overlap on the GPU.  The first call on a device must come before any stream
+    capture on it.
+    """
+    st = load().hss_layer_step_static(ctypes.byref(hss_dims.of(dims)), _ptr(P), _ptr(K_new),
+                                      _ptr(new_ids), int(num_new), _ptr(Q), int(rows_per_seq),
+                                      _ptr(Qp), _ptr(A_g), int(layer), _ptr(block_table),
+                                      _ptr(seq_offsets), int(num_seqs), int(total_blocks),
+                                      _ptr(scores), int(k), _ptr(victims), _ptr(dev_status),
+                                      _stream(stream))
+    _check(st, "hss_layer_step_static")
 
 
 def hss_read_device_error(stream=None) -> int:

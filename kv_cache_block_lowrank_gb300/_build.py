@@ -13,8 +13,9 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhss.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["hss_api.cu", "project_tc.cu", "score_decode.cu", "score_tc.cu", "rank.cu"]
-HEADERS = ["ptx.cuh", "internal.h"]
+SOURCES = ["hss_api.cu", "project_tc.cu", "score_decode.cu", "score_tc.cu", "rank.cu",
+           "no_alloc.cu"]
+HEADERS = ["ptx.cuh", "internal.h", "rank_device.cuh"]
 
 
 def nvcc() -> str:
