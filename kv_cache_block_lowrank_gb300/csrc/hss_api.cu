@@ -293,7 +293,7 @@ hss_status hss_layer_step(const hss_dims* dims, const uint16_t* P, const uint16_
     bool fused = false;
     if (total_blocks > 0) {
         if (decode) {
-            FusedRank fr{static_cast<int32_t*>(workspace), victims, k};
+            FusedRank fr{static_cast<int32_t*>(workspace), victims, k, true, new_ids, num_new};
             st = launch_score_decode(a, s, &fr, &fused);
         } else {
             st = launch_score_tc(a, s);

@@ -89,9 +89,15 @@ struct ScoreArgs {
 // Victim ranking fused into the decode scorer: counters are the caller's per-sequence
 // completion counters (zero on entry, left zero on exit).
 struct FusedRank {
-    int32_t* counters;
+    int32_t* counters;  // nullptr: no fused ranking
     int32_t* victims;
     int32_t k;
+    // The kernel launched just before the scorer on this stream writes only Qp and the A_g
+    // slots in new_ids (it is this call's own projection): the scorer may read the table
+    // and the other slots before its grid dependency wait.
+    bool early;
+    const int32_t* new_ids;
+    int64_t num_new;
 };
 // With fr != nullptr the ranking is fused when the shape allows; *fused reports whether it
 // was (otherwise the caller must rank separately).

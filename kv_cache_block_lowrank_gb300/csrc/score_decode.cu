@@ -58,9 +58,13 @@ struct DecodeParams {
     int32_t* victims;
     int32_t k;
     int32_t sel_cap;
-    int32_t keys_cap;
     int32_t frag_bytes_cta;  // offset of the ranking scratch in shared memory
     int32_t todo_cap;        // sequences one CTA can complete: its entry count
+    // early != 0: the previous kernel in the stream writes only Qp and the A_g slots listed
+    // in new_ids, so the rest may be read before the grid dependency wait.
+    const int32_t* new_ids;
+    int32_t num_new;
+    int32_t early;
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
@@ -101,25 +105,81 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
 
     const int64_t wid = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + warp;
     const int64_t i_begin = wid * p.entries_per_warp;
-    grid_dependency_wait();
-    grid_launch_dependents();
-    if (i_begin < p.total) {
+    const bool has_work = i_begin < p.total;
     const int64_t i_end = min(p.total, i_begin + p.entries_per_warp);
-
-    // Sequence of the first entry: the last s with seq_offsets[s] <= i_begin.
-    int lo = 0, hi = p.num_seqs;  // invariant: seq_offsets[lo] <= i_begin < seq_offsets[hi]
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (static_cast<int64_t>(__ldg(&p.seq_offsets[mid])) <= i_begin) lo = mid; else hi = mid;
-    }
-    int s = lo;
-    int64_t seq_end = __ldg(&p.seq_offsets[s + 1]);
-    int cached_seq = -1;
 
     const int tiles_per_head = p.bs >> 4;
     const int num_tiles = p.nkv * tiles_per_head;
     const int64_t slot_elems = static_cast<int64_t>(p.nkv) * p.bs * p.r;
     const int64_t tile_elems = 16 * static_cast<int64_t>(p.r);
+
+    // One batch of a slot's 16-token tiles, straight into MMA A-fragment registers.
+    uint32_t data[kTilesPerBatch][kRegsPerTile];
+    auto issue_loads = [&](const uint16_t* slot, int tb) {
+#pragma unroll
+        for (int u = 0; u < kTilesPerBatch; ++u) {
+            const int tile = tb + u;
+            if (tile < num_tiles) {
+                const uint16_t* base = slot + tile * tile_elems;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const uint16_t* rowp = base + (gq + 8 * half) * p.r;
+#pragma unroll
+                    for (int l = 0; l < kLoadsPerRow; ++l) {
+                        if constexpr (KSTEPS == 1) {
+                            const uint2 v = __ldcs(reinterpret_cast<const uint2*>(rowp + 4 * tq));
+                            data[u][half * 2 + 0] = v.x;
+                            data[u][half * 2 + 1] = v.y;
+                        } else {
+                            const uint4 v =
+                                __ldcs(reinterpret_cast<const uint4*>(rowp + 32 * l + 8 * tq));
+                            data[u][(half * kLoadsPerRow + l) * 4 + 0] = v.x;
+                            data[u][(half * kLoadsPerRow + l) * 4 + 1] = v.y;
+                            data[u][(half * kLoadsPerRow + l) * 4 + 2] = v.z;
+                            data[u][(half * kLoadsPerRow + l) * 4 + 3] = v.w;
+                        }
+                    }
+                }
+            }
+        }
+    };
+    auto find_seq = [&](int64_t i) {  // the last s with seq_offsets[s] <= i
+        int lo = 0, hi = p.num_seqs;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (static_cast<int64_t>(__ldg(&p.seq_offsets[mid])) <= i) lo = mid; else hi = mid;
+        }
+        return lo;
+    };
+
+    int s = 0;
+    int64_t seq_end = 0;
+    int32_t my_id = 0;
+    bool preloaded = false;
+    if (p.early && has_work) {
+        // The previous kernel in the stream is this call's own projection, which writes only
+        // Qp and the slots of new_ids: the offsets, the table and every other slot may be
+        // read before the dependency wait, so the first block's DRAM latency overlaps it.
+        s = find_seq(i_begin);
+        seq_end = __ldg(&p.seq_offsets[s + 1]);
+        const int64_t first_n = i_end - i_begin < 32 ? i_end - i_begin : 32;
+        my_id = lane < first_n ? __ldg(&p.table[i_begin + lane]) : 0;
+        const int32_t id0 = __shfl_sync(0xffffffffu, my_id, 0);
+        bool fresh = false;
+        for (int j = 0; j < p.num_new; ++j) fresh |= __ldg(&p.new_ids[j]) == id0;
+        if (id0 >= 0 && id0 < p.max_blocks && !fresh) {
+            issue_loads(p.A_g + (p.layer_slots + id0) * slot_elems, 0);
+            preloaded = true;
+        }
+    }
+    grid_dependency_wait();
+    grid_launch_dependents();
+    if (has_work) {
+    if (!p.early) {
+        s = find_seq(i_begin);
+        seq_end = __ldg(&p.seq_offsets[s + 1]);
+    }
+    int cached_seq = -1;
 
     // Column validity of this lane's accumulator entries (query vector index < nvec).
     bool col_ok[NT][2];
@@ -132,7 +192,7 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
     for (int64_t i0 = i_begin; i0 < i_end; i0 += 32) {
         const int64_t left = i_end - i0;
         const int n_here = left < 32 ? static_cast<int>(left) : 32;
-        const int32_t my_id = lane < n_here ? __ldg(&p.table[i0 + lane]) : 0;
+        if (!(p.early && i0 == i_begin)) my_id = lane < n_here ? __ldg(&p.table[i0 + lane]) : 0;
         for (int e = 0; e < n_here; ++e) {
             const int64_t i = i0 + e;
             while (i >= seq_end && s + 1 < p.num_seqs) {
@@ -150,37 +210,10 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
             const uint16_t* slot = p.A_g + (p.layer_slots + id) * slot_elems;
             float best = -INFINITY;
             for (int tb = 0; tb < num_tiles; tb += kTilesPerBatch) {
-                uint32_t data[kTilesPerBatch][kRegsPerTile];
-                // Issue every load of the batch first.
-#pragma unroll
-                for (int u = 0; u < kTilesPerBatch; ++u) {
-                    const int tile = tb + u;
-                    if (tile < num_tiles) {
-                        const uint16_t* base = slot + tile * tile_elems;
-#pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            const uint16_t* rowp = base + (gq + 8 * half) * p.r;
-#pragma unroll
-                            for (int l = 0; l < kLoadsPerRow; ++l) {
-                                if constexpr (KSTEPS == 1) {
-                                    const uint2 v = __ldcs(reinterpret_cast<const uint2*>(rowp + 4 * tq));
-                                    data[u][half * 2 + 0] = v.x;
-                                    data[u][half * 2 + 1] = v.y;
-                                } else {
-                                    const uint4 v = __ldcs(
-                                        reinterpret_cast<const uint4*>(rowp + 32 * l + 8 * tq));
-                                    data[u][(half * kLoadsPerRow + l) * 4 + 0] = v.x;
-                                    data[u][(half * kLoadsPerRow + l) * 4 + 1] = v.y;
-                                    data[u][(half * kLoadsPerRow + l) * 4 + 2] = v.z;
-                                    data[u][(half * kLoadsPerRow + l) * 4 + 3] = v.w;
-                                }
-                            }
-                        }
-                    }
-                }
+                // Issue every load of the batch first (the first one may already be in flight).
+                if (!(preloaded && i == i_begin && tb == 0)) issue_loads(slot, tb);
                 // (Re)fill the query-vector fragment cache while the loads are in flight.
                 if (s != cached_seq) {
-                    // Query-vector fragments of sequence s, in MMA B-fragment order.
                     __syncwarp();
                     for (int c = 0; c < p.nkv; ++c) {
 #pragma unroll
@@ -193,9 +226,10 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
                                     const int row = v / p.g;
                                     const int h = c * p.g + (v - row * p.g);
                                     const uint16_t* q =
-                                        p.Qp + ((static_cast<int64_t>(s) * p.rows + row) * p.nq + h) *
-                                                   p.r;
-                                    f = *reinterpret_cast<const uint2*>(q + frag_r_offset<KSTEPS>(ks, tq));
+                                        p.Qp +
+                                        ((static_cast<int64_t>(s) * p.rows + row) * p.nq + h) * p.r;
+                                    f = *reinterpret_cast<const uint2*>(
+                                        q + frag_r_offset<KSTEPS>(ks, tq));
                                 }
                                 cache[((c * KSTEPS + ks) * NT + nt) * 32 + lane] = f;
                             }
@@ -248,7 +282,7 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
             if (lane == 0) p.scores[i] = best;
         }
     }
-    }  // i_begin < total
+    }  // has_work
     if (p.counters == nullptr) return;
 
     // ---- fused ranking: the CTA that completes a sequence ranks it
@@ -256,8 +290,7 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
     uint8_t* rank_smem = smem_dec + p.frag_bytes_cta;
     uint64_t* sel = reinterpret_cast<uint64_t*>(rank_smem);
     rankdev::RankShared* sh = reinterpret_cast<rankdev::RankShared*>(sel + p.sel_cap);
-    uint32_t* keys = reinterpret_cast<uint32_t*>(sh + 1);
-    int* todo = reinterpret_cast<int*>(keys + p.keys_cap);  // [todo_cap + 1]
+    int* todo = reinterpret_cast<int*>(sh + 1);  // [todo_cap + 1]
     if (lane == 0) __threadfence();  // this warp's scores before the CTA's count
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -291,7 +324,7 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
         const int n = static_cast<int>(__ldg(&p.seq_offsets[q + 1]) - a);
         rankdev::rank_sequence<kThreadsFused>(p.scores + a, n, p.k,
                                               p.victims + static_cast<int64_t>(q) * p.k, sel,
-                                              p.sel_cap, sh, keys, p.keys_cap);
+                                              p.sel_cap, sh);
         if (threadIdx.x == 0) p.counters[q] = 0;  // ready for the next call
     }
     // Empty sequences have no entries to complete them: CTA 0 writes their -1 rows.
@@ -366,8 +399,15 @@ hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream, const Fu
     p.victims = nullptr;
     p.k = 0;
     p.sel_cap = 0;
-    p.keys_cap = 0;
     p.todo_cap = 0;
+    p.new_ids = nullptr;
+    p.num_new = 0;
+    p.early = 0;
+    if (fr != nullptr && fr->early && fr->num_new <= 64) {
+        p.new_ids = fr->new_ids;
+        p.num_new = static_cast<int32_t>(fr->num_new);
+        p.early = 1;
+    }
 
     const int fb = frag_bytes_per_warp(a);
     const int warps_per_cta = std::max(1, std::min(kWarpsMax, kFragBudgetBytes / fb));
@@ -380,18 +420,18 @@ hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream, const Fu
     const int grid = static_cast<int>((warps + warps_per_cta - 1) / warps_per_cta);
     // The ranking can ride along when a whole CTA of 8 warps is there to run it, every
     // sequence's keys fit in shared memory and the extra shared memory stays modest.
-    if (fr != nullptr && warps_per_cta == kWarpsMax && a.total <= rankdev::kKeysCap) {
+    // Long sequences are ranked by the dedicated kernel (1024 threads) instead.
+    if (fr != nullptr && fr->counters != nullptr && warps_per_cta == kWarpsMax &&
+        a.total <= kWarpsMax * 32 * rankdev::keys_per_thread<kWarpsMax * 32>()) {
         const int sel_cap = rankdev::rank_sel_cap(fr->k);
-        const int keys_cap = static_cast<int>(a.total);
         const int todo_cap = static_cast<int>(p.entries_per_warp * warps_per_cta);
-        const int extra = rankdev::rank_smem_bytes(sel_cap, keys_cap) + (todo_cap + 1) * 4;
+        const int extra = rankdev::rank_smem_bytes(sel_cap) + (todo_cap + 1) * 4;
         if (smem + extra <= 100 * 1024) {
             p.todo_cap = todo_cap;
             p.counters = fr->counters;
             p.victims = fr->victims;
             p.k = fr->k;
             p.sel_cap = sel_cap;
-            p.keys_cap = keys_cap;
             smem += extra;
             if (fused != nullptr) *fused = true;
         }

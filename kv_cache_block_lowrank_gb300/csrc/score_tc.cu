@@ -12,15 +12,17 @@
 // dot products with 256 query vectors: the max over query vectors is a per-thread register
 // reduction, and the max over a block's tokens is a 16-lane shuffle reduction.
 //
-// Work units: (sequence s, kv head c, slice of up to 1024 query vectors, 128-token tile).
-// A slice of Qp stays resident in shared memory (B operand, K-major, swizzled) while the
-// CTA streams token tiles; each CTA takes a contiguous run of units, so it reloads Qp only
-// when its run crosses into the next (s, c, slice).  Roles (persistent, 1 CTA per SM):
+// Work units: (sequence s, kv head c, 128-token tile) for one slice of up to 1024 query
+// vectors.  CTAs come in groups of `nslices`, one CTA per slice; the CTAs of a group walk the
+// same contiguous run of (s, c, tile) units in step, so each A tile is fetched from HBM once
+// and served from L2 to the group's other slices.  A CTA's slice of Qp stays resident in
+// shared memory (B operand, K-major, swizzled) and is reloaded only when its run crosses into
+// the next (s, c).  Roles (persistent, 1 CTA per SM):
 //   warp 0      TMA producer (Qp slices; per-block A_g boxes into a ring of stages)
 //   warp 1      TMEM allocator (512 columns) and MMA issuer, M=128, N=256, K=16 steps
-//   warps 2..9  epilogue, two warpgroups: warpgroup e drains accumulator buffer e, so one
-//               drains while the MMA fills the other; tcgen05.ld four 32-column loads per
-//               wait, 3-input max, block max by shuffles, one float atomic max per block
+//   warps 2..9  epilogue, two warpgroups that each drain half (128 columns) of every
+//               256-column accumulator chunk: four 32-column tcgen05.ld per wait, 3-input
+//               max, block max by shuffles, one float atomic max per block and warpgroup
 // Scores are first set to -inf (separate tiny kernel); every unit atomically maxes its
 // partial block maximum into the block's score.
 #include <cudaTypedefs.h>
@@ -76,8 +78,8 @@ struct TcParams {
     int32_t* lib_error;
     int64_t layer_slots;  // layer * max_blocks
     int64_t max_blocks;
-    int64_t total_units;
-    int64_t units_per_cta;
+    int64_t units_per_group;  // (s, c, tile) units per CTA group
+    int32_t num_groups;       // CTA groups; CTA b works on slice b % nslices of group b / nslices
     int32_t num_seqs;
     int32_t nkv;
     int32_t g;
@@ -103,8 +105,9 @@ struct Unit {
     int64_t pair;    // (s, c, q) identity
 };
 
-// Unit u -> (sequence, kv head, slice, tile), with units_before[s] = units of sequences < s.
-__device__ __forceinline__ Unit decode_unit(int64_t u, const TcParams& p,
+// Unit u -> (sequence, kv head, tile) for slice q, with units_before[s] = units of
+// sequences before s.
+__device__ __forceinline__ Unit decode_unit(int64_t u, int q, const TcParams& p,
                                             const int64_t* units_before) {
     int lo = 0, hi = p.num_seqs;  // last s with units_before[s] <= u
     while (hi - lo > 1) {
@@ -117,11 +120,11 @@ __device__ __forceinline__ Unit decode_unit(int64_t u, const TcParams& p,
     x.end = p.seq_offsets[lo + 1];
     const int64_t tiles = (x.end - x.first + p.bpt - 1) / p.bpt;
     const int64_t local = u - units_before[lo];
-    const int64_t pl = local / tiles;
-    x.t = local - pl * tiles;
-    x.c = static_cast<int>(pl / p.nslices);
-    x.q = static_cast<int>(pl - static_cast<int64_t>(x.c) * p.nslices);
-    x.pair = units_before[lo] + pl * tiles;  // unique per (s, c, q)
+    const int64_t c = local / tiles;
+    x.t = local - c * tiles;
+    x.c = static_cast<int>(c);
+    x.q = q;
+    x.pair = units_before[lo] + c * tiles;  // unique per (s, c); the slice is fixed per CTA
     return x;
 }
 
@@ -177,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < p.num_seqs; ++s) {
             units_before[s] = acc;
             const int64_t n = static_cast<int64_t>(p.seq_offsets[s + 1]) - p.seq_offsets[s];
-            acc += static_cast<int64_t>(p.nkv) * p.nslices * ((n + p.bpt - 1) / p.bpt);
+            acc += static_cast<int64_t>(p.nkv) * ((n + p.bpt - 1) / p.bpt);
         }
         units_before[p.num_seqs] = acc;
         for (int s = 0; s < p.stages; ++s) {
@@ -188,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(b_empty, 1);
         for (int a = 0; a < 2; ++a) {
             mbar_init(&t_full[a], 1);
-            mbar_init(&t_empty[a], 4);
+            mbar_init(&t_empty[a], 8);  // every epilogue warp drains part of each chunk
         }
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -198,9 +201,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
-    // The host sized the grid from an upper bound; the exact count is units_before[num_seqs].
-    const int64_t u_begin = static_cast<int64_t>(blockIdx.x) * p.units_per_cta;
-    const int64_t u_end = min(units_before[p.num_seqs], u_begin + p.units_per_cta);
+    // CTA b serves slice q = b % nslices for the units of group b / nslices.  The host sized
+    // the groups from an upper bound; the exact unit count is units_before[num_seqs].
+    const int q_slice = static_cast<int>(blockIdx.x % p.nslices);
+    const int64_t group = blockIdx.x / p.nslices;
+    const int64_t u_begin = group < p.num_groups ? group * p.units_per_group : 0;
+    const int64_t u_end = group < p.num_groups
+                              ? min(units_before[p.num_seqs], u_begin + p.units_per_group)
+                              : 0;
     const int nchunks = p.slice / kNChunk;
     const int elems_per_row = p.row_bytes / 2;
 
@@ -213,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int64_t prev_pair = -1, issued = 0;
             bool ok = true;
             for (int64_t u = u_begin; u < u_end && ok; ++u) {
-                const Unit x = decode_unit(u, p, units_before);
+                const Unit x = decode_unit(u, q_slice, p, units_before);
                 if (x.pair != prev_pair) {
                     if (prev_pair >= 0) {
                         ok = mbar_wait(b_empty, b_empty_phase);
@@ -279,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int64_t prev_pair = -1, it = 0;
             bool ok = true;
             for (int64_t u = u_begin; u < u_end && ok; ++u) {
-                const Unit x = decode_unit(u, p, units_before);
+                const Unit x = decode_unit(u, q_slice, p, units_before);
                 if (x.pair != prev_pair) {
                     if (prev_pair >= 0) umma_commit(b_empty);  // old slice free once MMAs finish
                     ok = mbar_wait(b_full, b_full_phase);
@@ -327,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // Epilogue: warpgroup eg drains accumulator buffer eg (every other N chunk); warp w
+        // Epilogue: warpgroup eg drains columns [128 eg, 128 eg + 128) of every chunk; warp w
         // owns TMEM lanes 32 * (w % 4) .. + 31 = token rows of the tile.
         const int eg = (warp - 2) >> 2;
         const int quarter = warp & 3;
@@ -335,31 +343,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t it = 0;  // global chunk counter, shared numbering with the MMA warp
         bool ok = true;
         for (int64_t u = u_begin; u < u_end && ok; ++u) {
-            const Unit x = decode_unit(u, p, units_before);
+            const Unit x = decode_unit(u, q_slice, p, units_before);
             float run = -INFINITY;
             bool any = false;
             for (int nc = 0; nc < nchunks; ++nc, ++it) {
-                if (static_cast<int>(it & 1) != eg) continue;
-                const int acc = eg;
+                const int acc = static_cast<int>(it & 1);
                 const bool got = mbar_wait(&t_full[acc], static_cast<uint32_t>((it >> 1) & 1));
                 if (__any_sync(0xffffffffu, !got) || *(volatile int*)abort_flag) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                any = true;
-                const int v0 = x.q * p.slice + nc * kNChunk;  // first query vector of the chunk
-                const int valid = min(kNChunk, p.nvec - v0);
-                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                       static_cast<uint32_t>(acc * kNChunk);
-                for (int half = 0; half < kNChunk; half += 128) {
+                const int col0 = eg * 128;
+                // Query vectors of this warpgroup's columns: v0 .. v0 + 127, valid below nvec.
+                const int v0 = x.q * p.slice + nc * kNChunk + col0;
+                const int valid = min(128, p.nvec - v0);
+                if (valid > 0) {
+                    any = true;
+                    const uint32_t taddr = tmem_base +
+                                           (static_cast<uint32_t>(quarter * 32) << 16) +
+                                           static_cast<uint32_t>(acc * kNChunk + col0);
                     uint32_t v[128];
-                    tmem_ld_32x32b_x32(taddr + half, v);
-                    tmem_ld_32x32b_x32(taddr + half + 32, v + 32);
-                    tmem_ld_32x32b_x32(taddr + half + 64, v + 64);
-                    tmem_ld_32x32b_x32(taddr + half + 96, v + 96);
+                    tmem_ld_32x32b_x32(taddr, v);
+                    tmem_ld_32x32b_x32(taddr + 32, v + 32);
+                    tmem_ld_32x32b_x32(taddr + 64, v + 64);
+                    tmem_ld_32x32b_x32(taddr + 96, v + 96);
                     tmem_ld_wait();
-                    if (half + 128 <= valid) {
+                    if (valid == 128) {
                         float m0 = run, m1 = run, m2 = run, m3 = run;
 #pragma unroll
                         for (int j = 0; j < 128; j += 8) {
@@ -372,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
 #pragma unroll
                         for (int j = 0; j < 128; ++j)
-                            if (half + j < valid) run = fmaxf(run, __uint_as_float(v[j]));
+                            if (j < valid) run = fmaxf(run, __uint_as_float(v[j]));
                     }
                 }
                 tc_fence_before_sync();
@@ -380,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&t_empty[acc]);
             }
             if (!ok) break;
-            if (!any) continue;  // no chunk of this unit landed in this warpgroup's buffer
+            if (!any) continue;  // none of this warpgroup's columns held a valid query vector
             // Max over the block's tokens: block_size consecutive lanes.
             for (int off = p.bs >> 1; off > 0; off >>= 1)
                 run = fmaxf(run, __shfl_xor_sync(0xffffffffu, run, off));
@@ -510,13 +520,17 @@ hss_status launch_score_tc(const ScoreArgs& a, cudaStream_t stream) {
     p.kchunks = L.kchunks;
     p.a_stage_bytes = L.a_stage_bytes;
     p.stages = L.stages;
-    // Unit count: exact for one sequence; otherwise an upper bound (the offsets live on the
-    // device), since every sequence contributes ceil(n_s / bpt) <= n_s / bpt + 1 tiles.
+    // Units per slice: exact for one sequence; otherwise an upper bound (the offsets live on
+    // the device), since every sequence contributes ceil(n_s / bpt) <= n_s / bpt + 1 tiles.
     const int64_t max_tiles = a.num_seqs == 1 ? (a.total + p.bpt - 1) / p.bpt
                                               : a.total / p.bpt + a.num_seqs;
-    p.total_units = static_cast<int64_t>(p.nkv) * p.nslices * max_tiles;
-    const int grid = static_cast<int>(std::min<int64_t>(dev->num_sms, p.total_units));
-    p.units_per_cta = (p.total_units + grid - 1) / grid;
+    const int64_t units = static_cast<int64_t>(p.nkv) * max_tiles;
+    // One CTA per SM, in groups of nslices (one CTA per slice).
+    int64_t groups = std::max<int64_t>(1, dev->num_sms / p.nslices);
+    groups = std::min<int64_t>(groups, units);
+    p.num_groups = static_cast<int32_t>(groups);
+    p.units_per_group = (units + groups - 1) / groups;
+    const int grid = static_cast<int>(groups * p.nslices);
 
     const int fill_grid = static_cast<int>(std::min<int64_t>((a.total + 255) / 256, 1024));
     float* scores = a.scores;
