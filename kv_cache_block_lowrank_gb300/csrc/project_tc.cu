@@ -125,24 +125,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Everything above is set-up that may overlap the previous kernel in the stream; global
     // memory is touched only after the dependency wait.
+    tc_fence_before_sync();
+    __syncthreads();  // barriers initialised, TMEM allocated
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
     grid_dependency_wait();
     grid_launch_dependents();
-    // P^T into shared memory, K-major with the 128-byte swizzle the MMA descriptor names:
-    // row j of chunk c holds P[64c .. 64c+63][j].  P is read with 16-byte loads, a batch of
-    // four per thread in flight at once, then scattered into the transposed layout.
-    {
+    if (warp != 0) {
+        // Warps 1..5 stage P^T while warp 0 already streams the first tiles in.  P^T goes
+        // into shared memory K-major with the 128-byte swizzle the MMA descriptor names:
+        // row j of chunk c holds P[64c .. 64c+63][j].  P is read with 16-byte loads, a batch
+        // of four per thread in flight at once, then scattered into the transposed layout.
+        constexpr int kStagers = kThreads - 32;
+        const int t = static_cast<int>(threadIdx.x) - 32;
         const int n16 = p.head_dim * r / 8;  // 16-byte chunks of P (8 consecutive j each)
         const uint4* P16 = reinterpret_cast<const uint4*>(p.P);
-        for (int base = threadIdx.x; base < n16; base += 4 * kThreads) {
+        for (int base = t; base < n16; base += 4 * kStagers) {
             uint4 v[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int e = base + u * kThreads;
+                const int e = base + u * kStagers;
                 if (e < n16) v[u] = __ldg(&P16[e]);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int e = base + u * kThreads;
+                const int e = base + u * kStagers;
                 if (e >= n16) continue;
                 const int d = (e * 8) / r, j0 = (e * 8) - d * r;
                 const int c = d / kChunkElems, kk = d - c * kChunkElems;
@@ -155,12 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        fence_proxy_async_smem();  // the generic-proxy P^T writes, visible to the tensor cores
+        // Named barrier 1 joins warps 1..5 only: the MMA warp starts once P^T is complete.
+        asm volatile("bar.sync 1, %0;" ::"n"(kThreads - 32) : "memory");
     }
-    fence_proxy_async_smem();  // make the generic-proxy P^T writes visible to the tensor cores
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
-    const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
         if (lane == 0) {

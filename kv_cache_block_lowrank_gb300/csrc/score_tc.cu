@@ -64,7 +64,8 @@ TcLayout make_tc_layout(int r, int smem_budget) {
     L.slice = std::min(kMaxSliceVecs, std::max(kNChunk, slice));
     L.b_bytes = L.slice * r * 2;
     L.a_stage_bytes = kTileTokens * r * 2;
-    const int fixed = 1024 + 512 + (kMaxSeqs + 1) * 8 + L.b_bytes;
+    // barriers (512) + units before each sequence (int64) + sequence offsets (int32)
+    const int fixed = 1024 + 512 + (kMaxSeqs + 1) * 8 + (kMaxSeqs + 1) * 4 + L.b_bytes;
     L.stages = std::min(4, (smem_budget - fixed) / L.a_stage_bytes);
     L.total_bytes = fixed + L.stages * L.a_stage_bytes;
     return L;
@@ -106,9 +107,9 @@ struct Unit {
 };
 
 // Unit u -> (sequence, kv head, tile) for slice q, with units_before[s] = units of
-// sequences before s.
+// sequences before s and offs = the sequence offsets, both cached in shared memory.
 __device__ __forceinline__ Unit decode_unit(int64_t u, int q, const TcParams& p,
-                                            const int64_t* units_before) {
+                                            const int64_t* units_before, const int32_t* offs) {
     int lo = 0, hi = p.num_seqs;  // last s with units_before[s] <= u
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -116,8 +117,8 @@ __device__ __forceinline__ Unit decode_unit(int64_t u, int q, const TcParams& p,
     }
     Unit x;
     x.s = lo;
-    x.first = p.seq_offsets[lo];
-    x.end = p.seq_offsets[lo + 1];
+    x.first = offs[lo];
+    x.end = offs[lo + 1];
     const int64_t tiles = (x.end - x.first + p.bpt - 1) / p.bpt;
     const int64_t local = u - units_before[lo];
     const int64_t c = local / tiles;
@@ -163,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
     int64_t* units_before = reinterpret_cast<int64_t*>(smem + p.b_bytes +
                                                        p.stages * p.a_stage_bytes + 512);
+    int32_t* offs = reinterpret_cast<int32_t*>(units_before + p.num_seqs + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -179,10 +181,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t acc = 0;
         for (int s = 0; s < p.num_seqs; ++s) {
             units_before[s] = acc;
+            offs[s] = p.seq_offsets[s];
             const int64_t n = static_cast<int64_t>(p.seq_offsets[s + 1]) - p.seq_offsets[s];
             acc += static_cast<int64_t>(p.nkv) * ((n + p.bpt - 1) / p.bpt);
         }
         units_before[p.num_seqs] = acc;
+        offs[p.num_seqs] = p.seq_offsets[p.num_seqs];
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&a_full[s], 1);
             mbar_init(&a_empty[s], 1);
@@ -221,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int64_t prev_pair = -1, issued = 0;
             bool ok = true;
             for (int64_t u = u_begin; u < u_end && ok; ++u) {
-                const Unit x = decode_unit(u, q_slice, p, units_before);
+                const Unit x = decode_unit(u, q_slice, p, units_before, offs);
                 if (x.pair != prev_pair) {
                     if (prev_pair >= 0) {
                         ok = mbar_wait(b_empty, b_empty_phase);
@@ -287,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int64_t prev_pair = -1, it = 0;
             bool ok = true;
             for (int64_t u = u_begin; u < u_end && ok; ++u) {
-                const Unit x = decode_unit(u, q_slice, p, units_before);
+                const Unit x = decode_unit(u, q_slice, p, units_before, offs);
                 if (x.pair != prev_pair) {
                     if (prev_pair >= 0) umma_commit(b_empty);  // old slice free once MMAs finish
                     ok = mbar_wait(b_full, b_full_phase);
@@ -343,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t it = 0;  // global chunk counter, shared numbering with the MMA warp
         bool ok = true;
         for (int64_t u = u_begin; u < u_end && ok; ++u) {
-            const Unit x = decode_unit(u, q_slice, p, units_before);
+            const Unit x = decode_unit(u, q_slice, p, units_before, offs);
             float run = -INFINITY;
             bool any = false;
             for (int nc = 0; nc < nchunks; ++nc, ++it) {
