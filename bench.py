@@ -180,6 +180,18 @@ def measured_peaks():
             "source": "fallback"}
 
 
+# ----------------------------------------------------------------------------- traffic
+# DRAM bytes per launch of each workload's dominant kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum) from the ncu captures summarised in profiles/, or None when the
+# kernel has changed since its capture.
+TRAFFIC = {
+    "decode": (16865792 + 0, "profiles/score_decode_layer_step.md"),
+    "batched": (283585024 + 2935808, "profiles/score_decode_batched.md"),
+    "prefill": (None, "profiles/score_tc_prefill.md: kernel changed since the capture"),
+    "ingest": (None, "profiles/project_ingest_40000_blocks.md: kernel changed since the capture"),
+}
+
+
 # ----------------------------------------------------------------------------- workloads
 
 class _Base:
@@ -835,7 +847,8 @@ def run_hss(args):
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": wl.dominant_bound, "kernel": wl.dominant_kernel,
                          "achieved": achieved, "peak": peak, "unit": unit,
-                         "frac": achieved / peak, "traffic": None, "peak_source": peak_src,
+                         "frac": achieved / peak, "traffic": TRAFFIC[args.workload][0],
+                         "traffic_source": TRAFFIC[args.workload][1], "peak_source": peak_src,
                          "launch_us": dom_s * 1e6, "work_per_launch": wl.dominant_units,
                          "how": "CUDA events around graph replays of back-to-back launches of "
                                 "this kernel on its launching stream (gaps between graph nodes "

@@ -158,6 +158,27 @@ hss_status hss_score_blocks(const hss_dims* dims, const uint16_t* Qp, int32_t ro
                             const int32_t* seq_offsets, int32_t num_seqs, int64_t total_blocks,
                             float* scores, int32_t path, int32_t* dev_status, void* stream);
 
+/*
+ * Block scores restricted to visible tokens: hss_score_blocks with two optional masks.
+ * Token t of the entry at table position j of sequence s (j counted from seq_offsets[s])
+ * sits at position p = j * block_size + t.
+ *   ctx_len   device, [num_seqs] int32, or NULL: only tokens with p < ctx_len[s] count
+ *             (the tail of a partly filled last block, or blocks past the context);
+ *   row_pos0  device, [num_seqs] int32, or NULL: causal mask for a chunk of query rows
+ *             whose first row sits at row_pos0[s]; row r sees only p <= row_pos0[s] + r.
+ * A block with no visible candidate scores -inf.  Both NULL: exactly hss_score_blocks.
+ * The predictor page's scorer takes no lengths or positions (Predictor::score_blocks);
+ * these masks are the next step it leaves open.  Seeing a key only from rows at or after
+ * its position follows the complete-block count of "metrale_model_layers/layers/
+ * qsa_select.rs" (QsaIndexer::prefill_select).
+ */
+hss_status hss_score_blocks_masked(const hss_dims* dims, const uint16_t* Qp, int32_t rows_per_seq,
+                                   const uint16_t* A_g, int32_t layer, const int32_t* block_table,
+                                   const int32_t* seq_offsets, int32_t num_seqs,
+                                   int64_t total_blocks, const int32_t* ctx_len,
+                                   const int32_t* row_pos0, float* scores, int32_t path,
+                                   int32_t* dev_status, void* stream);
+
 /* Largest k that hss_rank_victims accepts. */
 #define HSS_MAX_VICTIMS 8192
 

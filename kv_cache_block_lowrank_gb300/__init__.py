@@ -40,6 +40,7 @@ EXPORTED = (
     "hss_status_string", "hss_version", "hss_validate_dims", "hss_a_g_bytes", "hss_project_q",
     "hss_project_kv_blocks", "hss_score_blocks", "hss_rank_victims", "hss_read_device_error",
     "hss_layer_step", "hss_layer_step_workspace_bytes", "hss_layer_step_static",
+    "hss_score_blocks_masked",
     "hss_layer_step_static_max_seqs",
 )
 
@@ -101,6 +102,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.hss_project_kv_blocks.argtypes = [dp, vp, vp, i32, vp, i64, vp, vp, vp]
     lib.hss_score_blocks.restype = i32
     lib.hss_score_blocks.argtypes = [dp, vp, i32, vp, i32, vp, vp, i32, i64, vp, i32, vp, vp]
+    lib.hss_score_blocks_masked.restype = i32
+    lib.hss_score_blocks_masked.argtypes = [dp, vp, i32, vp, i32, vp, vp, i32, i64, vp, vp, vp,
+                                            i32, vp, vp]
     lib.hss_rank_victims.restype = i32
     lib.hss_rank_victims.argtypes = [vp, vp, i32, i64, i32, vp, vp]
     lib.hss_read_device_error.restype = i32
@@ -187,6 +191,20 @@ def hss_score_blocks(dims, Qp, rows_per_seq: int, A_g, layer: int, block_table, 
                                  int(num_seqs), int(total_blocks), _ptr(scores), int(path),
                                  _ptr(dev_status), _stream(stream))
     _check(st, "hss_score_blocks")
+
+
+def hss_score_blocks_masked(dims, Qp, rows_per_seq: int, A_g, layer: int, block_table,
+                            seq_offsets, num_seqs: int, total_blocks: int, ctx_len, row_pos0,
+                            scores, path: int = HSS_PATH_AUTO, dev_status=None,
+                            stream=None) -> None:
+    """hss_score_blocks over visible tokens only (length mask ctx_len, causal row_pos0)."""
+    st = load().hss_score_blocks_masked(ctypes.byref(hss_dims.of(dims)), _ptr(Qp),
+                                        int(rows_per_seq), _ptr(A_g), int(layer),
+                                        _ptr(block_table), _ptr(seq_offsets), int(num_seqs),
+                                        int(total_blocks), _ptr(ctx_len), _ptr(row_pos0),
+                                        _ptr(scores), int(path), _ptr(dev_status),
+                                        _stream(stream))
+    _check(st, "hss_score_blocks_masked")
 
 
 def hss_rank_victims(scores, seq_offsets, num_seqs: int, total_blocks: int, k: int, victims,

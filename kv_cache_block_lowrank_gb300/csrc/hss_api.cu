@@ -145,6 +145,17 @@ hss_status hss_score_blocks(const hss_dims* dims, const uint16_t* Qp, int32_t ro
                             const uint16_t* A_g, int32_t layer, const int32_t* block_table,
                             const int32_t* seq_offsets, int32_t num_seqs, int64_t total_blocks,
                             float* scores, int32_t path, int32_t* dev_status, void* stream) {
+    return hss_score_blocks_masked(dims, Qp, rows_per_seq, A_g, layer, block_table, seq_offsets,
+                                   num_seqs, total_blocks, nullptr, nullptr, scores, path,
+                                   dev_status, stream);
+}
+
+hss_status hss_score_blocks_masked(const hss_dims* dims, const uint16_t* Qp, int32_t rows_per_seq,
+                                   const uint16_t* A_g, int32_t layer, const int32_t* block_table,
+                                   const int32_t* seq_offsets, int32_t num_seqs,
+                                   int64_t total_blocks, const int32_t* ctx_len,
+                                   const int32_t* row_pos0, float* scores, int32_t path,
+                                   int32_t* dev_status, void* stream) {
     hss_status st = check_dims(dims);
     if (st != HSS_OK) return st;
     if (layer < 0 || layer >= dims->num_layers) return HSS_ERR_OUT_OF_RANGE;
@@ -174,6 +185,8 @@ hss_status hss_score_blocks(const hss_dims* dims, const uint16_t* Qp, int32_t ro
     a.r = dims->r;
     a.block_size = dims->block_size;
     a.dev_status = dev_status;
+    a.ctx_len = ctx_len;
+    a.row_pos0 = row_pos0;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t nvec = static_cast<int64_t>(rows_per_seq) * (dims->num_q_heads / dims->num_kv_heads);
     int chosen = path;

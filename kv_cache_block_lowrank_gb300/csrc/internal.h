@@ -85,6 +85,11 @@ struct ScoreArgs {
     int32_t r;
     int32_t block_size;
     int32_t* dev_status;
+    // Optional masks (device int32 per sequence, nullptr = off): only tokens at position
+    // p < ctx_len[s] count; with row_pos0, row r only sees p <= row_pos0[s] + r.  Token t of
+    // the entry at table position j of its sequence sits at p = j * block_size + t.
+    const int32_t* ctx_len = nullptr;
+    const int32_t* row_pos0 = nullptr;
 };
 // Victim ranking fused into the decode scorer: counters are the caller's per-sequence
 // completion counters (zero on entry, left zero on exit).

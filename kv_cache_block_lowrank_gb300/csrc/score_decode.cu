@@ -65,6 +65,10 @@ struct DecodeParams {
     const int32_t* new_ids;
     int32_t num_new;
     int32_t early;
+    // Optional masks (nullptr = off): token position p = j * bs + t for the entry at table
+    // position j of its sequence; p < ctx_len[s]; causal: p <= row_pos0[s] + row.
+    const int32_t* ctx_len;
+    const int32_t* row_pos0;
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
@@ -156,6 +160,7 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
     int64_t seq_end = 0;
     int32_t my_id = 0;
     bool preloaded = false;
+    const bool masked = p.ctx_len != nullptr || p.row_pos0 != nullptr;
     if (p.early && has_work) {
         // The previous kernel in the stream is this call's own projection, which writes only
         // Qp and the slots of new_ids: the offsets, the table and every other slot may be
@@ -180,6 +185,12 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
         seq_end = __ldg(&p.seq_offsets[s + 1]);
     }
     int cached_seq = -1;
+    int64_t seq_begin = masked ? __ldg(&p.seq_offsets[s]) : 0;
+    int64_t clen = INT64_MAX, pos0 = INT64_MAX / 2;
+    if (masked) {
+        if (p.ctx_len != nullptr) clen = __ldg(&p.ctx_len[s]);
+        if (p.row_pos0 != nullptr) pos0 = __ldg(&p.row_pos0[s]);
+    }
 
     // Column validity of this lane's accumulator entries (query vector index < nvec).
     bool col_ok[NT][2];
@@ -198,6 +209,11 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
             while (i >= seq_end && s + 1 < p.num_seqs) {
                 ++s;
                 seq_end = __ldg(&p.seq_offsets[s + 1]);
+                if (masked) {
+                    seq_begin = __ldg(&p.seq_offsets[s]);
+                    if (p.ctx_len != nullptr) clen = __ldg(&p.ctx_len[s]);
+                    if (p.row_pos0 != nullptr) pos0 = __ldg(&p.row_pos0[s]);
+                }
             }
             const int32_t id = __shfl_sync(0xffffffffu, my_id, e);
             if (id < 0 || id >= p.max_blocks) {
@@ -268,10 +284,31 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
                                 mma_bf16_16816(acc[nt], a0, a1, a2, a3, b.x, b.y);
                             }
                         }
+                        if (!masked) {
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            if (col_ok[nt][0]) best = fmaxf(best, fmaxf(acc[nt][0], acc[nt][2]));
-                            if (col_ok[nt][1]) best = fmaxf(best, fmaxf(acc[nt][1], acc[nt][3]));
+                            for (int nt = 0; nt < NT; ++nt) {
+                                if (col_ok[nt][0])
+                                    best = fmaxf(best, fmaxf(acc[nt][0], acc[nt][2]));
+                                if (col_ok[nt][1])
+                                    best = fmaxf(best, fmaxf(acc[nt][1], acc[nt][3]));
+                            }
+                        } else {
+                            // Accumulator rows are tokens gq and gq + 8 of this 16-token tile,
+                            // columns are query vectors (row = vector / g).
+                            const int mt = tile - c * tiles_per_head;
+                            const int64_t p_lo = (i - seq_begin) * p.bs + mt * 16 + gq;
+                            const int64_t p_hi = p_lo + 8;
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                                for (int cc = 0; cc < 2; ++cc) {
+                                    if (!col_ok[nt][cc]) continue;
+                                    const int64_t lim = min(clen - 1,
+                                                            pos0 + (nt * 8 + 2 * tq + cc) / p.g);
+                                    if (p_lo <= lim) best = fmaxf(best, acc[nt][cc]);
+                                    if (p_hi <= lim) best = fmaxf(best, acc[nt][cc + 2]);
+                                }
+                            }
                         }
                     }
                 }
@@ -403,6 +440,8 @@ hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream, const Fu
     p.new_ids = nullptr;
     p.num_new = 0;
     p.early = 0;
+    p.ctx_len = a.ctx_len;
+    p.row_pos0 = a.row_pos0;
     if (fr != nullptr && fr->early && fr->num_new <= 64) {
         p.new_ids = fr->new_ids;
         p.num_new = static_cast<int32_t>(fr->num_new);

@@ -96,6 +96,8 @@ struct TcParams {
     int32_t b_bytes;
     int32_t a_stage_bytes;
     int32_t stages;
+    const int32_t* ctx_len;   // optional masks, see ScoreArgs
+    const int32_t* row_pos0;
 };
 
 struct Unit {
@@ -350,6 +352,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Unit x = decode_unit(u, q_slice, p, units_before, offs);
             float run = -INFINITY;
             bool any = false;
+            // This thread's token position; with masks, the token may be hidden (past the
+            // context) or visible only to query rows from some row on (causal).
+            const int64_t tok_pos =
+                (x.t * p.bpt + token / p.bs) * static_cast<int64_t>(p.bs) + (token % p.bs);
+            const bool tok_ok = p.ctx_len == nullptr || tok_pos < __ldg(&p.ctx_len[x.s]);
+            // First visible query vector: rows r >= tok_pos - row_pos0, i.e. vectors from
+            // (tok_pos - row_pos0) * g on.
+            const int64_t first_vec =
+                p.row_pos0 == nullptr ? 0 : (tok_pos - __ldg(&p.row_pos0[x.s])) * p.g;
             for (int nc = 0; nc < nchunks; ++nc, ++it) {
                 const int acc = static_cast<int>(it & 1);
                 const bool got = mbar_wait(&t_full[acc], static_cast<uint32_t>((it >> 1) & 1));
@@ -373,7 +384,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_32x32b_x32(taddr + 64, v + 64);
                     tmem_ld_32x32b_x32(taddr + 96, v + 96);
                     tmem_ld_wait();
-                    if (valid == 128) {
+                    const int64_t lo64 = first_vec - v0;
+                    const int lo_col = lo64 <= 0 ? 0 : (lo64 >= 128 ? 128 : static_cast<int>(lo64));
+                    if (!tok_ok || lo_col >= valid) {
+                        // nothing visible in these columns
+                    } else if (lo_col > 0) {
+#pragma unroll
+                        for (int j = 0; j < 128; ++j)
+                            if (j >= lo_col && j < valid) run = fmaxf(run, __uint_as_float(v[j]));
+                    } else if (valid == 128) {
                         float m0 = run, m1 = run, m2 = run, m3 = run;
 #pragma unroll
                         for (int j = 0; j < 128; j += 8) {
@@ -524,6 +543,8 @@ hss_status launch_score_tc(const ScoreArgs& a, cudaStream_t stream) {
     p.kchunks = L.kchunks;
     p.a_stage_bytes = L.a_stage_bytes;
     p.stages = L.stages;
+    p.ctx_len = a.ctx_len;
+    p.row_pos0 = a.row_pos0;
     // Units per slice: exact for one sequence; otherwise an upper bound (the offsets live on
     // the device), since every sequence contributes ceil(n_s / bpt) <= n_s / bpt + 1 tiles.
     const int64_t max_tiles = a.num_seqs == 1 ? (a.total + p.bpt - 1) / p.bpt

@@ -70,6 +70,10 @@ def _bind(path: str):
     lib.orc_score_entries.restype = _i64
     lib.orc_score_entries.argtypes = [_u16p, _i64, _int, _int, _int, _int, _int, _u16p, _i64,
                                       _i64, _i32p, _i64p, _i64p, _i64, _f64p, _f64p]
+    lib.orc_score_blocks_masked.restype = _i64
+    lib.orc_score_blocks_masked.argtypes = [_u16p, _i64, _int, _int, _int, _int, _int, _u16p,
+                                            _i64, _i64, _i32p, _i64p, ctypes.c_void_p,
+                                            ctypes.c_void_p, _f64p, _f64p, _int]
     lib.orc_rank_victims.restype = _int
     lib.orc_rank_victims.argtypes = [_f32p, _i64p, _i64, _int, _i32p]
     return lib
@@ -198,6 +202,34 @@ def score_entries(Qp: np.ndarray, A_g: np.ndarray, layer: int, block_table: np.n
     tsum = np.empty(ent.size, dtype=np.float64)
     bad = L.orc_score_entries(Qp.reshape(-1), S, R, nq, nkv, r, bs, _u16(A_g).reshape(-1), layer,
                               mb, table, offs, ent, ent.size, score, tsum)
+    return score, tsum, int(bad)
+
+
+def score_blocks_masked(Qp: np.ndarray, A_g: np.ndarray, layer: int, block_table: np.ndarray,
+                        seq_offsets: np.ndarray, ctx_len=None, row_pos0=None, nthreads: int = 1,
+                        L=None):
+    """score_blocks restricted to visible candidates.
+
+    Token t of table position j (within its sequence) sits at p = j * block_size + t.
+    ctx_len[s] (optional): only tokens with p < ctx_len[s] count.  row_pos0[s] (optional,
+    causal): query row `row` sees tokens with p <= row_pos0[s] + row.  A block with no
+    visible candidate scores -inf.
+    """
+    L = L or lib()
+    Qp = _u16(Qp)
+    S, R, nq, r = Qp.shape
+    nl, mb, nkv, bs, r2 = A_g.shape
+    table = np.ascontiguousarray(block_table, dtype=np.int32)
+    offs = np.ascontiguousarray(seq_offsets, dtype=np.int64)
+    cl = None if ctx_len is None else np.ascontiguousarray(ctx_len, dtype=np.int64)
+    rp = None if row_pos0 is None else np.ascontiguousarray(row_pos0, dtype=np.int64)
+    total = int(offs[-1])
+    score = np.empty(total, dtype=np.float64)
+    tsum = np.empty(total, dtype=np.float64)
+    bad = L.orc_score_blocks_masked(Qp.reshape(-1), S, R, nq, nkv, r, bs, _u16(A_g).reshape(-1),
+                                    layer, mb, table, offs,
+                                    None if cl is None else cl.ctypes.data,
+                                    None if rp is None else rp.ctypes.data, score, tsum, nthreads)
     return score, tsum, int(bad)
 
 

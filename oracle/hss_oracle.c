@@ -414,6 +414,130 @@ int64_t orc_score_entries(const uint16_t* Qp, int64_t num_seqs, int rows_per_seq
 }
 
 /* ------------------------------------------------------------------------ */
+/* Step 3b: block scores with a valid-length mask and a causal mask          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The same score as orc_score_blocks, restricted to the visible candidates.
+ * Token t of the block at table position j of sequence s (j counted from the
+ * sequence's first entry) sits at position p = j * block_size + t.
+ *   ctx_len  (NULL: no length mask)  token p is scored only if p < ctx_len[s];
+ *   row_pos0 (NULL: no causal mask)  query row `row` sees token p only if
+ *                                    p <= row_pos0[s] + row.
+ * A block with no visible candidate scores -inf (tsum 0); an out-of-range id
+ * still scores +inf.
+ */
+static void orc_score_one_masked(const orc_score_shape* k, int64_t s, int64_t id, int64_t j,
+                                 const int64_t* ctx_len, const int64_t* row_pos0, double* score,
+                                 double* tsum)
+{
+    if (id < 0 || id >= k->max_blocks) {
+        *score = INFINITY;
+        *tsum = 0.0;
+        return;
+    }
+    int g = k->nq / k->nkv;
+    int64_t slot_elems = (int64_t)k->nkv * k->bs * k->r;
+    const uint16_t* slot = k->A + (k->layer * k->max_blocks + id) * slot_elems;
+    double best = -INFINITY;
+    double best_abs = 0.0;
+    for (int row = 0; row < k->rows; ++row) {
+        for (int h = 0; h < k->nq; ++h) {
+            const uint16_t* q = k->Qp + ((s * k->rows + row) * (int64_t)k->nq + h) * k->r;
+            int c_kv = h / g;
+            for (int t = 0; t < k->bs; ++t) {
+                int64_t pos = j * k->bs + t;
+                if (ctx_len != NULL && pos >= ctx_len[s]) {
+                    continue;
+                }
+                if (row_pos0 != NULL && pos > row_pos0[s] + row) {
+                    continue;
+                }
+                const uint16_t* a = slot + ((int64_t)c_kv * k->bs + t) * k->r;
+                double dot = 0.0, mag = 0.0;
+                for (int jj = 0; jj < k->r; ++jj) {
+                    double term = orc_bf16_to_double(q[jj]) * orc_bf16_to_double(a[jj]);
+                    dot += term;
+                    mag += fabs(term);
+                }
+                if (dot > best) {
+                    best = dot;
+                }
+                if (mag > best_abs) {
+                    best_abs = mag;
+                }
+            }
+        }
+    }
+    *score = best;
+    *tsum = best_abs;
+}
+
+typedef struct {
+    orc_score_shape shape;
+    const int32_t* table;
+    const int64_t* seq_of_entry;
+    const int64_t* seq_offsets;
+    const int64_t* ctx_len;
+    const int64_t* row_pos0;
+    double* score;
+    double* tsum;
+} orc_masked_ctx;
+
+static void orc_masked_item(void* c, int64_t i)
+{
+    orc_masked_ctx* k = (orc_masked_ctx*)c;
+    int64_t s = k->seq_of_entry[i];
+    orc_score_one_masked(&k->shape, s, k->table[i], i - k->seq_offsets[s], k->ctx_len, k->row_pos0,
+                         &k->score[i], &k->tsum[i]);
+}
+
+int64_t orc_score_blocks_masked(const uint16_t* Qp, int64_t num_seqs, int rows_per_seq,
+                                int num_q_heads, int num_kv_heads, int r, int block_size,
+                                const uint16_t* A_g, int64_t layer, int64_t max_blocks,
+                                const int32_t* block_table, const int64_t* seq_offsets,
+                                const int64_t* ctx_len, const int64_t* row_pos0, double* score,
+                                double* tsum, int nthreads)
+{
+    int64_t total = seq_offsets[num_seqs];
+    int64_t* seq_of_entry = (int64_t*)malloc(sizeof(int64_t) * (size_t)(total > 0 ? total : 1));
+    if (seq_of_entry == NULL) {
+        return -1;
+    }
+    for (int64_t s = 0; s < num_seqs; ++s) {
+        for (int64_t i = seq_offsets[s]; i < seq_offsets[s + 1]; ++i) {
+            seq_of_entry[i] = s;
+        }
+    }
+    orc_masked_ctx k;
+    k.shape.Qp = Qp;
+    k.shape.A = A_g;
+    k.shape.layer = layer;
+    k.shape.max_blocks = max_blocks;
+    k.shape.rows = rows_per_seq;
+    k.shape.nq = num_q_heads;
+    k.shape.nkv = num_kv_heads;
+    k.shape.r = r;
+    k.shape.bs = block_size;
+    k.table = block_table;
+    k.seq_of_entry = seq_of_entry;
+    k.seq_offsets = seq_offsets;
+    k.ctx_len = ctx_len;
+    k.row_pos0 = row_pos0;
+    k.score = score;
+    k.tsum = tsum;
+    orc_parallel_for(total, nthreads, orc_masked_item, &k);
+    free(seq_of_entry);
+    int64_t bad = 0;
+    for (int64_t i = 0; i < total; ++i) {
+        if (block_table[i] < 0 || block_table[i] >= max_blocks) {
+            ++bad;
+        }
+    }
+    return bad;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Step 4: eviction victims (ascending score; lower index first on ties)    */
 /* ------------------------------------------------------------------------ */
 

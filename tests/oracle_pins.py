@@ -309,6 +309,100 @@ def pin_victims_brute_force(L):
         assert got[si].tolist() == exp
 
 
+def _masked_case(rng, *, nq=4, nkv=2, hd=32, bs=4, S=3, R=3, lengths=(5, 0, 7), pool=16):
+    Q, K, ids, table, offs = _grid_case(rng, nq=nq, nkv=nkv, hd=hd, bs=bs, S=S, R=R,
+                                        lengths=list(lengths), layers=1, layer=0, pool=pool)
+    P = to_bf16_bits(np.eye(hd))
+    A = np.zeros((1, pool, nkv, bs, hd), dtype=np.uint16)
+    return Q, K, ids, table, offs, P, A
+
+
+def pin_masked_brute_force(L):
+    """Length and causal masks against a numpy brute force over explicit token positions."""
+    rng = np.random.default_rng(31)
+    nq, nkv, hd, bs, S, R = 4, 2, 32, 4, 3, 3
+    Q, K, ids, table, offs, P, A = _masked_case(rng, nq=nq, nkv=nkv, hd=hd, bs=bs, S=S, R=R)
+    oracle.project_kv_blocks(P, K, 0, ids, A, L=L)
+    Qp = oracle.project_q(Q, P, L=L)
+    ctx = np.array([17, 3, 25])          # seq 0: 5 blocks = 20 tokens, 17 valid
+    pos0 = np.array([9, 0, 12])
+    Kd = {int(b): from_bf16_bits(K[i]) for i, b in enumerate(ids)}
+    Qf = from_bf16_bits(Q)
+    g = nq // nkv
+    for use_len, use_causal in ((True, False), (False, True), (True, True)):
+        got, _, _ = oracle.score_blocks_masked(Qp, A, 0, table, offs,
+                                               ctx_len=ctx if use_len else None,
+                                               row_pos0=pos0 if use_causal else None, L=L)
+        exp = []
+        for sq in range(S):
+            for i in range(int(offs[sq]), int(offs[sq + 1])):
+                j = i - int(offs[sq])
+                kb = Kd[int(table[i])]
+                best = -math.inf
+                for row in range(R):
+                    for h in range(nq):
+                        for t in range(bs):
+                            p = j * bs + t
+                            if use_len and p >= ctx[sq]:
+                                continue
+                            if use_causal and p > pos0[sq] + row:
+                                continue
+                            best = max(best, float(Qf[sq, row, h] @ kb[t, h // g]))
+                exp.append(best)
+        assert np.array_equal(got, np.array(exp)), (use_len, use_causal)
+
+
+def pin_masked_reduces_to_unmasked(L):
+    """A length covering every token and row positions past the context change nothing;
+    hiding everything gives -inf; a longer context never lowers a score."""
+    rng = np.random.default_rng(32)
+    Q, K, ids, table, offs, P, A = _masked_case(rng)
+    oracle.project_kv_blocks(P, K, 0, ids, A, L=L)
+    Qp = oracle.project_q(Q, P, L=L)
+    base, tb, _ = oracle.score_blocks(Qp, A, 0, table, offs, L=L)
+    lens = np.diff(offs) * 4
+    full, tf, _ = oracle.score_blocks_masked(Qp, A, 0, table, offs, ctx_len=lens,
+                                             row_pos0=np.full(3, 10 ** 6), L=L)
+    assert np.array_equal(full, base) and np.array_equal(tf, tb)
+    none, tn, _ = oracle.score_blocks_masked(Qp, A, 0, table, offs, ctx_len=np.zeros(3),
+                                             L=L)
+    assert np.all(np.isneginf(none)) and not tn.any()
+    hidden, _, _ = oracle.score_blocks_masked(Qp, A, 0, table, offs, row_pos0=np.full(3, -3),
+                                              L=L)
+    assert np.all(np.isneginf(hidden))  # row r sees p <= -3 + r < 0 for r < 3
+    prev = None
+    for c in range(0, 30, 3):
+        cur, _, _ = oracle.score_blocks_masked(Qp, A, 0, table, offs, ctx_len=np.full(3, c),
+                                               L=L)
+        if prev is not None:
+            assert np.all(cur >= prev)
+        prev = cur
+
+
+def pin_masked_hand_case(L):
+    """Hand case: block_size 2, two query rows at positions 1 and 2 (causal, row_pos0 = 1).
+    Block 0 (positions 0, 1) is seen by both rows; of block 1 (positions 2, 3) only row 1
+    sees position 2, and nobody sees position 3."""
+    P = to_bf16_bits(np.eye(16))
+    Q = np.zeros((1, 2, 1, 16))
+    Q[0, :, 0, 0] = 1.0                          # both rows: the first coordinate
+    K = np.zeros((2, 2, 1, 16))
+    K[0, 0, 0, 0], K[0, 1, 0, 0] = 3.0, -1.0     # block 0 tokens: dots 3, -1
+    K[1, 0, 0, 0], K[1, 1, 0, 0] = 0.5, 7.0      # block 1 tokens: dots 0.5 (row 1 only), 7
+    A = np.zeros((1, 2, 1, 2, 16), dtype=np.uint16)
+    oracle.project_kv_blocks(P, to_bf16_bits(K), 0, np.array([0, 1]), A, L=L)
+    Qp = oracle.project_q(to_bf16_bits(Q), P, L=L)
+    sc, _, _ = oracle.score_blocks_masked(Qp, A, 0, np.array([0, 1]), np.array([0, 2]),
+                                          row_pos0=np.array([1]), L=L)
+    assert sc.tolist() == [3.0, 0.5], sc
+    sc, _, _ = oracle.score_blocks_masked(Qp, A, 0, np.array([0, 1]), np.array([0, 2]),
+                                          ctx_len=np.array([1]), L=L)
+    assert sc[0] == 3.0 and math.isinf(sc[1]) and sc[1] < 0
+    sc, _, _ = oracle.score_blocks_masked(Qp, A, 0, np.array([1, 0]), np.array([0, 2]),
+                                          ctx_len=np.array([3]), L=L)
+    assert sc.tolist() == [7.0, 3.0], sc     # table order decides positions
+
+
 ALL_PINS = [
     pin_bf16_hand_values,
     pin_bf16_matches_torch,
@@ -321,4 +415,7 @@ ALL_PINS = [
     pin_out_of_range,
     pin_victim_order,
     pin_victims_brute_force,
+    pin_masked_brute_force,
+    pin_masked_reduces_to_unmasked,
+    pin_masked_hand_case,
 ]

@@ -57,6 +57,14 @@ MUTANTS = [
      "victims[s * (int64_t)k + j] = j < n ? keyed[j].idx : 0;", 0),
     ("bad_id_scored_zero", "*score = INFINITY;\n        *tsum = 0.0;",
      "*score = 0.0;\n        *tsum = 0.0;", 0),
+    ("length_mask_off_by_one", "if (ctx_len != NULL && pos >= ctx_len[s]) {",
+     "if (ctx_len != NULL && pos > ctx_len[s]) {", 0),
+    ("causal_mask_off_by_one", "if (row_pos0 != NULL && pos > row_pos0[s] + row) {",
+     "if (row_pos0 != NULL && pos >= row_pos0[s] + row) {", 0),
+    ("causal_ignores_row", "if (row_pos0 != NULL && pos > row_pos0[s] + row) {",
+     "if (row_pos0 != NULL && pos > row_pos0[s]) {", 0),
+    ("position_not_per_sequence", "i - k->seq_offsets[s], k->ctx_len",
+     "i, k->ctx_len", 0),
 ]
 
 
