@@ -266,6 +266,16 @@ hss_status hss_layer_step_static(const hss_dims* dims, const uint16_t* P, const 
                                  int32_t* victims, int32_t* dev_status, void* stream);
 
 /*
+ * Failure-detection self-test.  Every pipeline wait in the tensor-core kernels gives up
+ * after a time limit and reports HSS_ERR_DEVICE_TIMEOUT instead of hanging the GPU.  This
+ * call launches one small kernel whose thread waits, with that same bounded wait, on a
+ * barrier nothing arrives on, for limit_ns (1e3 .. 2e9) nanoseconds; the kernel then stores
+ * HSS_ERR_DEVICE_TIMEOUT into *dev_status (device int32, which the caller zeroes first) and
+ * into the library's error word, and exits.  The context stays usable.
+ */
+hss_status hss_self_test_wait_timeout(int32_t* dev_status, int64_t limit_ns, void* stream);
+
+/*
  * Device-side error word of the current device: the first HSS_ERR_* code a
  * kernel raised since the last read (HSS_ERR_DEVICE_TIMEOUT when a pipeline
  * wait ran out), or HSS_OK.  Synchronises `stream`, copies the word to

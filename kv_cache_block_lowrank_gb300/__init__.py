@@ -41,7 +41,7 @@ EXPORTED = (
     "hss_project_kv_blocks", "hss_score_blocks", "hss_rank_victims", "hss_read_device_error",
     "hss_layer_step", "hss_layer_step_workspace_bytes", "hss_layer_step_static",
     "hss_score_blocks_masked",
-    "hss_layer_step_static_max_seqs",
+    "hss_layer_step_static_max_seqs", "hss_self_test_wait_timeout",
 )
 
 
@@ -105,6 +105,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.hss_score_blocks_masked.restype = i32
     lib.hss_score_blocks_masked.argtypes = [dp, vp, i32, vp, i32, vp, vp, i32, i64, vp, vp, vp,
                                             i32, vp, vp]
+    lib.hss_self_test_wait_timeout.restype = i32
+    lib.hss_self_test_wait_timeout.argtypes = [vp, i64, vp]
     lib.hss_rank_victims.restype = i32
     lib.hss_rank_victims.argtypes = [vp, vp, i32, i64, i32, vp, vp]
     lib.hss_read_device_error.restype = i32
@@ -254,6 +256,12 @@ def hss_layer_step_static(dims, P, K_new, new_ids, num_new: int, Q, rows_per_seq
                                       _ptr(scores), int(k), _ptr(victims), _ptr(dev_status),
                                       _stream(stream))
     _check(st, "hss_layer_step_static")
+
+
+def hss_self_test_wait_timeout(dev_status, limit_ns: int, stream=None) -> None:
+    """Launch a kernel whose bounded pipeline wait runs out (it sets dev_status)."""
+    st = load().hss_self_test_wait_timeout(_ptr(dev_status), int(limit_ns), _stream(stream))
+    _check(st, "hss_self_test_wait_timeout")
 
 
 def hss_read_device_error(stream=None) -> int:

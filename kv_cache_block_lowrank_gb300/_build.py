@@ -14,7 +14,7 @@ OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhss.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["hss_api.cu", "project_tc.cu", "score_decode.cu", "score_tc.cu", "rank.cu",
-           "no_alloc.cu"]
+           "no_alloc.cu", "selftest.cu"]
 HEADERS = ["ptx.cuh", "internal.h", "rank_device.cuh"]
 
 

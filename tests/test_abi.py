@@ -179,3 +179,10 @@ def test_layer_step_validation(lib):
     assert status_of(hss.hss_layer_step, *base(num_new=-1)) == hss.HSS_ERR_INVALID_ARGUMENT
     assert status_of(hss.hss_layer_step, *base(d=dims(num_kv_heads=3))) == \
         hss.HSS_ERR_INVALID_DIMS
+
+
+def test_self_test_validation(lib):
+    assert status_of(hss.hss_self_test_wait_timeout, None, 1_000_000, 0) == hss.HSS_ERR_NULL_POINTER
+    assert status_of(hss.hss_self_test_wait_timeout, FAKE, 10, 0) == hss.HSS_ERR_INVALID_ARGUMENT
+    assert status_of(hss.hss_self_test_wait_timeout, FAKE, 3 * 10 ** 9, 0) == \
+        hss.HSS_ERR_INVALID_ARGUMENT
