@@ -92,7 +92,9 @@ __device__ __forceinline__ int frag_r_offset(int ks, int t) {
     }
 }
 
-template <int KSTEPS, int NT>
+// MASKED: the call passed ctx_len or row_pos0.  A template parameter, so the unmasked kernel
+// carries none of the mask arithmetic.
+template <int KSTEPS, int NT, bool MASKED>
 __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(16) uint8_t smem_dec[];
     uint2* frag_cache_all = reinterpret_cast<uint2*>(smem_dec);
@@ -160,7 +162,6 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
     int64_t seq_end = 0;
     int32_t my_id = 0;
     bool preloaded = false;
-    const bool masked = p.ctx_len != nullptr || p.row_pos0 != nullptr;
     if (p.early && has_work) {
         // The previous kernel in the stream is this call's own projection, which writes only
         // Qp and the slots of new_ids: the offsets, the table and every other slot may be
@@ -185,9 +186,9 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
         seq_end = __ldg(&p.seq_offsets[s + 1]);
     }
     int cached_seq = -1;
-    int64_t seq_begin = masked ? __ldg(&p.seq_offsets[s]) : 0;
+    int64_t seq_begin = MASKED ? __ldg(&p.seq_offsets[s]) : 0;
     int64_t clen = INT64_MAX, pos0 = INT64_MAX / 2;
-    if (masked) {
+    if (MASKED) {
         if (p.ctx_len != nullptr) clen = __ldg(&p.ctx_len[s]);
         if (p.row_pos0 != nullptr) pos0 = __ldg(&p.row_pos0[s]);
     }
@@ -209,7 +210,7 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
             while (i >= seq_end && s + 1 < p.num_seqs) {
                 ++s;
                 seq_end = __ldg(&p.seq_offsets[s + 1]);
-                if (masked) {
+                if (MASKED) {
                     seq_begin = __ldg(&p.seq_offsets[s]);
                     if (p.ctx_len != nullptr) clen = __ldg(&p.ctx_len[s]);
                     if (p.row_pos0 != nullptr) pos0 = __ldg(&p.row_pos0[s]);
@@ -284,7 +285,7 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
                                 mma_bf16_16816(acc[nt], a0, a1, a2, a3, b.x, b.y);
                             }
                         }
-                        if (!masked) {
+                        if (!MASKED) {
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt) {
                                 if (col_ok[nt][0])
@@ -377,7 +378,9 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
 template <int KSTEPS, int NT>
 hss_status launch_t(const DecodeParams& p, int warps_per_cta, int smem, int grid,
                     cudaStream_t stream) {
-    auto k = score_decode_kernel<KSTEPS, NT>;
+    const bool masked = p.ctx_len != nullptr || p.row_pos0 != nullptr;
+    auto k = masked ? score_decode_kernel<KSTEPS, NT, true>
+                    : score_decode_kernel<KSTEPS, NT, false>;
     if (smem > 48 * 1024) {
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
             cudaSuccess)

@@ -148,6 +148,9 @@ __global__ void fill_neg_inf(float* __restrict__ x, int64_t n) {
         x[i] = -INFINITY;
 }
 
+// MASKED: the call passed ctx_len or row_pos0.  A template parameter, so the unmasked kernel
+// carries none of the mask arithmetic.
+template <bool MASKED>
 __global__ void __launch_bounds__(kThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_q, const TcParams p) {
@@ -354,13 +357,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool any = false;
             // This thread's token position; with masks, the token may be hidden (past the
             // context) or visible only to query rows from some row on (causal).
-            const int64_t tok_pos =
-                (x.t * p.bpt + token / p.bs) * static_cast<int64_t>(p.bs) + (token % p.bs);
-            const bool tok_ok = p.ctx_len == nullptr || tok_pos < __ldg(&p.ctx_len[x.s]);
-            // First visible query vector: rows r >= tok_pos - row_pos0, i.e. vectors from
-            // (tok_pos - row_pos0) * g on.
-            const int64_t first_vec =
-                p.row_pos0 == nullptr ? 0 : (tok_pos - __ldg(&p.row_pos0[x.s])) * p.g;
+            bool tok_ok = true;
+            int64_t first_vec = 0;
+            if (MASKED) {
+                const int64_t tok_pos =
+                    (x.t * p.bpt + token / p.bs) * static_cast<int64_t>(p.bs) + (token % p.bs);
+                tok_ok = p.ctx_len == nullptr || tok_pos < __ldg(&p.ctx_len[x.s]);
+                // First visible query vector: rows r >= tok_pos - row_pos0, i.e. vectors from
+                // (tok_pos - row_pos0) * g on.
+                first_vec = p.row_pos0 == nullptr ? 0 : (tok_pos - __ldg(&p.row_pos0[x.s])) * p.g;
+            }
             for (int nc = 0; nc < nchunks; ++nc, ++it) {
                 const int acc = static_cast<int>(it & 1);
                 const bool got = mbar_wait(&t_full[acc], static_cast<uint32_t>((it >> 1) & 1));
@@ -384,11 +390,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_32x32b_x32(taddr + 64, v + 64);
                     tmem_ld_32x32b_x32(taddr + 96, v + 96);
                     tmem_ld_wait();
-                    const int64_t lo64 = first_vec - v0;
-                    const int lo_col = lo64 <= 0 ? 0 : (lo64 >= 128 ? 128 : static_cast<int>(lo64));
-                    if (!tok_ok || lo_col >= valid) {
+                    int lo_col = 0;
+                    if (MASKED) {
+                        const int64_t lo64 = first_vec - v0;
+                        lo_col = lo64 <= 0 ? 0 : (lo64 >= 128 ? 128 : static_cast<int>(lo64));
+                    }
+                    if (MASKED && (!tok_ok || lo_col >= valid)) {
                         // nothing visible in these columns
-                    } else if (lo_col > 0) {
+                    } else if (MASKED && lo_col > 0) {
 #pragma unroll
                         for (int j = 0; j < 128; ++j)
                             if (j >= lo_col && j < valid) run = fmaxf(run, __uint_as_float(v[j]));
@@ -514,7 +523,11 @@ hss_status launch_score_tc(const ScoreArgs& a, cudaStream_t stream) {
         std::lock_guard<std::mutex> lk(g_smem_mu);
         const int d = dev->device & 63;
         if (g_smem_set[d] < L.total_bytes) {
-            if (cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(score_tc_kernel<false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     L.total_bytes) != cudaSuccess ||
+                cudaFuncSetAttribute(score_tc_kernel<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      L.total_bytes) != cudaSuccess)
                 return HSS_ERR_CUDA;
             g_smem_set[d] = L.total_bytes;
@@ -563,8 +576,9 @@ hss_status launch_score_tc(const ScoreArgs& a, cudaStream_t stream) {
     if (launch_pdl(fill_neg_inf, dim3(fill_grid), dim3(256), 0, stream, scores, total) !=
         cudaSuccess)
         return HSS_ERR_CUDA;
-    if (launch_pdl(score_tc_kernel, dim3(grid), dim3(kThreads), L.total_bytes, stream, tmap_a,
-                   tmap_q, p) != cudaSuccess)
+    const bool masked = a.ctx_len != nullptr || a.row_pos0 != nullptr;
+    if (launch_pdl(masked ? score_tc_kernel<true> : score_tc_kernel<false>, dim3(grid),
+                   dim3(kThreads), L.total_bytes, stream, tmap_a, tmap_q, p) != cudaSuccess)
         return HSS_ERR_CUDA;
     return HSS_OK;
 }
