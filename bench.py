@@ -571,16 +571,30 @@ class IngestWorkload(_Base):
     l2_note = "no flush: each step reads 4 GiB of K and 512 MiB of A_g, far above the 129 MB L2"
 
     def e2e_setup(self):
-        self.h_vic = self.torch.empty(1, self.k, dtype=self.torch.int32).pin_memory()
+        # Every step's new key blocks (all 32 layers, 4 GiB) and the query come from pinned
+        # host memory, layer by layer, into the device buffers the step projects from.
+        torch = self.torch
+        self.h_K = [k.cpu().pin_memory() for k in self.K]
+        self.h_Q = self.Q.cpu().pin_memory()
+        self.h_vic = torch.empty(1, self.k, dtype=torch.int32).pin_memory()
 
     def e2e_step(self):
-        self.step()
+        hss, d = self.hss, self.dims
+        nb = self.new_ids.numel()
+        for l in range(self.L):
+            self.K[l].copy_(self.h_K[l], non_blocking=True)
+            hss.hss_project_kv_blocks(d, self.P, self.K[l], l, self.new_ids, nb, self.A)
+        self.Q.copy_(self.h_Q, non_blocking=True)
+        hss.hss_project_q(d, self.P, self.Q, 1, self.Qp)
+        hss.hss_score_blocks(d, self.Qp, 1, self.A, self.layer, self.table, self.offs, 1, self.n,
+                             self.scores)
+        hss.hss_rank_victims(self.scores, self.offs, 1, self.n, self.k, self.victims)
         self.h_vic.copy_(self.victims, non_blocking=True)
         self.torch.cuda.current_stream().synchronize()
 
     @property
     def e2e_bytes(self):
-        return 0, self.k * 4
+        return sum(k.numel() for k in self.K) * 2 + self.Q.numel() * 2, self.k * 4
 
 
 WORKLOADS = {"decode": DecodeWorkload, "batched": BatchedWorkload, "prefill": PrefillWorkload,
