@@ -10,9 +10,10 @@
 //      runs 8-bit digits from the first bit where keys differ, and stops as soon as the
 //      chosen bin holds exactly the keys still needed (block scores cluster, so this skips
 //      most of the passes a fixed 4 x 8-bit select would make);
-//   3. collection: every key <= the threshold is appended with warp-aggregated atomics (the
-//      sort below orders ties by index); when a mass of keys ties at the threshold and they
-//      would not fit, an ordered pass takes the first ones by index instead;
+//   3. collection: every key <= the threshold goes to the selection, placed by per-warp
+//      ballot counts and one scan over the warps (streamed keys: warp-aggregated atomics);
+//      the sort below orders ties by index.  When a mass of keys ties at the threshold and
+//      they would not fit, an ordered pass takes the first ones by index instead;
 //   4. a bitonic sort of the selected words: stages whose partner is in another warp go
 //      through shared memory, stages within a warp run in registers with shuffles.
 #pragma once
@@ -181,13 +182,13 @@ __device__ void rank_with(const float* __restrict__ sc, int n, int k, int32_t* _
     const uint32_t lane_lt = (1u << lane) - 1u;
     const int take = n < k ? n : k;
 
+    KeySet<THREADS, IN_REGS> ks;
+    ks.load(sc, n);  // the loads are in flight while the histograms are cleared
     if (tid < 256) {
         sh->hist[0][tid] = 0;
         sh->hist[1][tid] = 0;
     }
     if (tid == 0) sh->count_sel = 0;
-    KeySet<THREADS, IN_REGS> ks;
-    ks.load(sc, n);
     __syncthreads();  // the zeroed histogram and counter before anyone adds to them
 
     // Warp-aggregated append of (key, index) to sel.
@@ -218,6 +219,49 @@ __device__ void rank_with(const float* __restrict__ sc, int n, int k, int32_t* _
                 const int i = j * THREADS + tid;
                 fn(i < n, ks.slot_key(j), i);
             }
+        }
+    };
+
+    // Every key with pred(key) goes to sel.  With the keys in registers the positions come
+    // from per-warp ballot counts and one scan over the warps (no atomics, one barrier);
+    // streamed keys use the warp-aggregated append.  The order in sel is irrelevant: the
+    // words are sorted afterwards.
+    auto collect = [&](auto&& pred) {
+        if constexpr (IN_REGS) {
+            constexpr int kK = KeySet<THREADS, IN_REGS>::kKpt;
+            const int rounds = (n + THREADS - 1) / THREADS;
+            // The ballots are taken twice (count, then place) rather than kept in registers.
+            uint32_t wcount = 0;
+#pragma unroll
+            for (int j = 0; j < kK; ++j) {
+                if (j < rounds) {  // uniform: every lane of every warp takes the same branches
+                    const int i = j * THREADS + tid;
+                    wcount += __popc(__ballot_sync(0xffffffffu, i < n && pred(ks.r[j])));
+                }
+            }
+            if (lane == 0) sh->warp_tot[warp] = wcount;
+            __syncthreads();
+            uint32_t base = 0;
+            for (int w = 0; w < warp; ++w) base += sh->warp_tot[w];
+#pragma unroll
+            for (int j = 0; j < kK; ++j) {
+                if (j < rounds) {
+                    const int i = j * THREADS + tid;
+                    const bool pick = i < n && pred(ks.r[j]);
+                    const uint32_t ball = __ballot_sync(0xffffffffu, pick);
+                    if (pick) {
+                        const uint32_t pos = base + __popc(ball & lane_lt);
+                        if (pos < static_cast<uint32_t>(sel_cap))
+                            sel[pos] = (static_cast<uint64_t>(ks.r[j]) << 32) |
+                                       static_cast<uint32_t>(i);
+                    }
+                    base += __popc(ball);
+                }
+            }
+        } else {
+            for_each_uniform([&](bool valid, uint32_t key, int i) {
+                append(valid && pred(key), key, i);
+            });
         }
     };
 
@@ -324,7 +368,7 @@ __device__ void rank_with(const float* __restrict__ sc, int n, int k, int32_t* _
 
         if (n_lt + n_eq <= sel_cap) {
             // ---- 3a. every key <= T; the sort orders ties at T by index
-            for_each_uniform([&](bool valid, uint32_t key, int i) { append(valid && key <= T, key, i); });
+            collect([&](uint32_t key) { return key <= T; });
             count = n_lt + n_eq;
         } else {
             // ---- 3b. ordered: keys < T, then the first `need` keys == T by index
@@ -351,7 +395,7 @@ __device__ void rank_with(const float* __restrict__ sc, int n, int k, int32_t* _
             count = take;
         }
     } else {
-        for_each_uniform([&](bool valid, uint32_t key, int i) { append(valid, key, i); });
+        collect([](uint32_t) { return true; });
         count = n;
     }
 
