@@ -259,7 +259,9 @@ class DecodeWorkload(_Base):
         K_new = self.K_new[l] if K_new is None else K_new
         Q = self.Q[l] if Q is None else Q
         if not self.unfused:
-            hss.hss_layer_step(d, self.P, K_new, self.new_ids, 1, Q, 1, self.Qp[l], self.A, l,
+            # Qp = NULL: the caller wants scores and victims, not the projected queries, so the
+            # decode scorer projects them itself.
+            hss.hss_layer_step(d, self.P, K_new, self.new_ids, 1, Q, 1, None, self.A, l,
                                self.table, self.offs, 1, self.n, self.scores[l], self.k,
                                self.victims[l], self.ws, self.ws_bytes)
             return
@@ -291,7 +293,8 @@ class DecodeWorkload(_Base):
                 f"{d.block_size}, 1 sequence of {self.n * d.block_size} tokens ({self.n} blocks, "
                 f"permuted table), 1 query row, bottom-{self.k}; per layer call: project the "
                 f"block being written, project Q, score, rank"
-                + (" (four calls)" if self.unfused else " (hss_layer_step: 2 launches)"))
+                + (" (four calls)" if self.unfused else
+                   " (hss_layer_step, queries projected in the scorer: 2 launches)"))
 
     l2_note = ("no flush: each step reads 32 x 16 MiB = 512 MiB of A_g, above the 129 MB L2, "
                "so every layer call reads cold A_g")

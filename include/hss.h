@@ -214,7 +214,21 @@ hss_status hss_rank_victims(const float* scores, const int32_t* seq_offsets, int
  *   K_new, new_ids, num_new  blocks written this step (num_new may be 0), as in
  *                            hss_project_kv_blocks
  *   Q                        device, [num_seqs, rows_per_seq, num_q_heads, head_dim] bf16
- *   Qp                       device, [num_seqs, rows_per_seq, num_q_heads, r] bf16 (output)
+ *   Qp                       device, [num_seqs, rows_per_seq, num_q_heads, r] bf16 (output),
+ *                            or NULL when the caller does not need the projected queries.
+ *                            With NULL, the decode scorer projects the queries itself (into
+ *                            shared memory; Qp is never stored), so the scoring path has one
+ *                            launch fewer: only the new blocks are projected before it, and it
+ *                            waits for that projection only where it reads a new block.  NULL
+ *                            is accepted when the call takes the decode scorer (rows_per_seq *
+ *                            num_q_heads / num_kv_heads <= 16), num_seqs <= 8, and the query
+ *                            rows, P and the projected fragments fit the scorer's 96 KiB of
+ *                            shared memory (the Llama-3-8B-like decode layer, 32 q / 8 kv
+ *                            heads, head_dim 128, r 32, one row, needs 22 KiB); otherwise the
+ *                            call returns HSS_ERR_NULL_POINTER.  The scores then come from
+ *                            the same fp32-accumulated, bf16-rounded Qp, summed in another
+ *                            order, so a Qp element may differ from hss_project_q's by one
+ *                            bf16 ulp.
  *   scores, victims          outputs, as in hss_score_blocks / hss_rank_victims
  *   workspace                device, >= hss_layer_step_workspace_bytes(num_seqs) bytes,
  *                            4-byte aligned: per-sequence completion counters.  Zero it once
@@ -245,7 +259,8 @@ hss_status hss_layer_step(const hss_dims* dims, const uint16_t* P, const uint16_
  * words (16 KiB) on every GPU that loads it, kept until the process exits.  It allocates
  * nothing and calls no allocating routine.
  *
- *   Arguments and results: as hss_layer_step, without workspace / workspace_bytes.
+ *   Arguments and results: as hss_layer_step, without workspace / workspace_bytes; Qp must
+ *   not be NULL here (HSS_ERR_NULL_POINTER).
  *   num_seqs > HSS_LAYER_STEP_STATIC_MAX_SEQS  -> HSS_ERR_WORKSPACE_TOO_SMALL, nothing enqueued.
  *   Each call first clears the counters it uses (a memset on `stream`), then runs the same
  *   kernels as hss_layer_step.

@@ -235,8 +235,7 @@ hss_status hss_layer_step(const hss_dims* dims, const uint16_t* P, const uint16_
     if (num_seqs == 0 && total_blocks != 0) return HSS_ERR_INVALID_ARGUMENT;
     if (P == nullptr || A_g == nullptr) return HSS_ERR_NULL_POINTER;
     if (num_new > 0 && (K_new == nullptr || new_ids == nullptr)) return HSS_ERR_NULL_POINTER;
-    if (num_seqs > 0 && (Q == nullptr || Qp == nullptr || seq_offsets == nullptr ||
-                         victims == nullptr))
+    if (num_seqs > 0 && (Q == nullptr || seq_offsets == nullptr || victims == nullptr))
         return HSS_ERR_NULL_POINTER;
     if (total_blocks > 0 && (block_table == nullptr || scores == nullptr))
         return HSS_ERR_NULL_POINTER;
@@ -276,6 +275,12 @@ hss_status hss_layer_step(const hss_dims* dims, const uint16_t* P, const uint16_
         static_cast<int64_t>(rows_per_seq) * (dims->num_q_heads / dims->num_kv_heads);
     const bool decode = nvec <= 16 && score_decode_supported(a);
     if (total_blocks > 0 && !decode && !score_tc_supported(a)) return HSS_ERR_UNSUPPORTED_SHAPE;
+    // Qp == NULL: the caller does not want the projected queries, and the decode scorer
+    // projects them itself (one launch fewer on the scoring path).
+    const bool inline_q = Qp == nullptr && num_seqs > 0;
+    if (inline_q && total_blocks > 0 &&
+        !(decode && score_decode_inline_supported(a, dims->head_dim)))
+        return HSS_ERR_NULL_POINTER;
 
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     // 1. one launch projects the query rows and the newly written blocks
@@ -300,14 +305,23 @@ hss_status hss_layer_step(const hss_dims* dims, const uint16_t* P, const uint16_
     kv.max_blocks = dims->max_blocks;
     kv.layer = layer;
     kv.dev_status = dev_status;
+    if (inline_q) q.num_rows = 0;  // only the new blocks
     st = launch_project2(q, &kv, s);
     if (st != HSS_OK || num_seqs == 0) return st;
     // 2. scores, with the ranking fused into the decode scorer where it fits
     bool fused = false;
     if (total_blocks > 0) {
         if (decode) {
-            FusedRank fr{static_cast<int32_t*>(workspace), victims, k, true, new_ids, num_new};
-            st = launch_score_decode(a, s, &fr, &fused);
+            // The kernel just before the scorer is this call's projection unless the queries
+            // are projected in the scorer and there are no new blocks: then nothing of this
+            // call precedes it and it may read nothing before its dependency wait.
+            const bool own_projection = !inline_q || num_new > 0;
+            FusedRank fr{static_cast<int32_t*>(workspace), victims, k, own_projection, new_ids,
+                         num_new};
+            // With the queries projected in the scorer, that projection writes only the new
+            // slots, so the scorer need not wait for it anywhere else.
+            const InlineQ iq{Q, P, dims->head_dim, num_new > 0};
+            st = launch_score_decode(a, s, &fr, &fused, inline_q ? &iq : nullptr);
         } else {
             st = launch_score_tc(a, s);
         }

@@ -104,11 +104,23 @@ struct FusedRank {
     const int32_t* new_ids;
     int64_t num_new;
 };
+// Queries projected inside the decode scorer (a.Qp unused): Q [num_seqs, rows, nq, hd] and
+// P [hd, r].  nowait: the kernel just before the scorer is this call's projection of the
+// fr->new_ids slots alone (fr->num_new <= 32), so only warps reading those slots wait for it.
+struct InlineQ {
+    const uint16_t* Q;
+    const uint16_t* P;
+    int32_t head_dim;
+    bool nowait;
+};
 // With fr != nullptr the ranking is fused when the shape allows; *fused reports whether it
-// was (otherwise the caller must rank separately).
+// was (otherwise the caller must rank separately).  With iq != nullptr the queries are
+// projected in the scorer; score_decode_inline_supported must hold.
 hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream,
-                               const FusedRank* fr = nullptr, bool* fused = nullptr);
+                               const FusedRank* fr = nullptr, bool* fused = nullptr,
+                               const InlineQ* iq = nullptr);
 bool score_decode_supported(const ScoreArgs& a);
+bool score_decode_inline_supported(const ScoreArgs& a, int32_t head_dim);
 hss_status launch_score_tc(const ScoreArgs& a, cudaStream_t stream);
 bool score_tc_supported(const ScoreArgs& a);
 

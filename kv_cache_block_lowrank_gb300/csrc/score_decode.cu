@@ -30,6 +30,10 @@ namespace {
 
 constexpr int kWarpsMax = 8;
 constexpr int kFragBudgetBytes = 48 * 1024;  // per CTA, all warps' fragment caches
+// In-kernel query projection: at most this many sequences per call (every CTA projects all of
+// them) and this much shared memory for their fragment caches, P's fragments and Q's rows.
+constexpr int kInlineMaxSeqs = 8;
+constexpr int kInlineBudgetBytes = 96 * 1024;
 
 struct DecodeParams {
     const uint16_t* Qp;
@@ -69,6 +73,18 @@ struct DecodeParams {
     // position j of its sequence; p < ctx_len[s]; causal: p <= row_pos0[s] + row.
     const int32_t* ctx_len;
     const int32_t* row_pos0;
+    // INLINE kernels project the queries themselves (Qp is never stored): every CTA projects
+    // Q [num_seqs, rows, nq, hd] through P [hd, r] straight into a shared-memory cache of
+    // MMA B fragments, one per sequence.  Shared memory: that cache (cache_bytes), P's
+    // fragments (r * hd * 2 bytes), then Q's rows (row stride hd + 32 elements).
+    const uint16_t* Q;
+    const uint16_t* P;
+    int32_t hd;
+    int32_t cache_bytes;
+    // nowait != 0 (INLINE only): the previous kernel in the stream is this call's projection
+    // of the new_ids slots and nothing else, so only a warp about to read one of those slots
+    // takes the grid dependency wait; num_new <= 32 then.
+    int32_t nowait;
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
@@ -93,8 +109,8 @@ __device__ __forceinline__ int frag_r_offset(int ks, int t) {
 }
 
 // MASKED: the call passed ctx_len or row_pos0.  A template parameter, so the unmasked kernel
-// carries none of the mask arithmetic.
-template <int KSTEPS, int NT, bool MASKED>
+// carries none of the mask arithmetic.  INLINE: the queries are projected in the kernel.
+template <int KSTEPS, int NT, bool MASKED, bool INLINE>
 __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(16) uint8_t smem_dec[];
     uint2* frag_cache_all = reinterpret_cast<uint2*>(smem_dec);
@@ -178,8 +194,110 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
             preloaded = true;
         }
     }
-    grid_dependency_wait();
+    const bool nowait = INLINE && p.nowait != 0;
+    if (!nowait) grid_dependency_wait();
     grid_launch_dependents();
+    // nowait: this lane's new id (lane < num_new <= 32); a warp waits before its first one.
+    const int32_t my_new = nowait && lane < p.num_new ? __ldg(&p.new_ids[lane]) : -1;
+    bool waited = !nowait;
+
+    if constexpr (INLINE) {
+        // The first block's loads go out before the projection below, so their DRAM latency
+        // covers it (without this call's own projection before the scorer they could not be
+        // issued before the dependency wait).
+        if (has_work && !preloaded) {
+            s = find_seq(i_begin);
+            seq_end = __ldg(&p.seq_offsets[s + 1]);
+            const int64_t first_n = i_end - i_begin < 32 ? i_end - i_begin : 32;
+            my_id = lane < first_n ? __ldg(&p.table[i_begin + lane]) : 0;
+            const int32_t id0 = __shfl_sync(0xffffffffu, my_id, 0);
+            if (id0 >= 0 && id0 < p.max_blocks && !__any_sync(0xffffffffu, my_new == id0)) {
+                issue_loads(p.A_g + (p.layer_slots + id0) * slot_elems, 0);
+                preloaded = true;
+            }
+        }
+        // ---- project every sequence's queries into the CTA's fragment cache
+        // Staging, one coalesced round trip: P as MMA B fragments and Q's rows.  The
+        // head_dim coordinates are visited in the order that makes each lane's 16-byte load
+        // of a query row its A fragment for two k-steps (the scheme the slot loads use for
+        // r), so B takes the same order: fragment entry (n-tile np, 32-wide chunk l, lane)
+        // holds P[32l + 8t + e][8np + g] as its e-th bf16 (t = lane % 4, g = lane / 4).
+        uint4* pfrag = reinterpret_cast<uint4*>(smem_dec + p.cache_bytes);
+        uint16_t* pfrag_h = reinterpret_cast<uint16_t*>(pfrag);
+        uint16_t* qs = reinterpret_cast<uint16_t*>(smem_dec + p.cache_bytes + p.r * p.hd * 2);
+        const int qstride = p.hd + 32;  // padded rows: conflict-free fragment reads
+        const int lchunks = p.hd >> 5;
+        const int M = p.rows * p.nq;
+        for (int z = threadIdx.x; z < p.cache_bytes / 16; z += blockDim.x)
+            reinterpret_cast<uint4*>(smem_dec)[z] = make_uint4(0u, 0u, 0u, 0u);
+        const int pvec = p.r >> 3;  // 16-byte pieces per row of P
+        for (int e = threadIdx.x; e < p.hd * pvec; e += blockDim.x) {
+            const int dd = e / pvec, jc = e - dd * pvec;
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.P + dd * p.r) + jc);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            const int base = ((jc * lchunks + (dd >> 5)) * 32 + ((dd & 31) >> 3)) * 8 + (dd & 7);
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj)  // column 8 jc + jj sits in lane group jj
+                pfrag_h[base + jj * 32] = static_cast<uint16_t>(w[jj >> 1] >> ((jj & 1) * 16));
+        }
+        const int qvec = p.hd >> 3;
+        for (int e = threadIdx.x; e < p.num_seqs * M * qvec; e += blockDim.x) {
+            const int row = e / qvec, c8 = e - row * qvec;
+            reinterpret_cast<uint4*>(qs + row * qstride)[c8] = __ldg(
+                reinterpret_cast<const uint4*>(p.Q + static_cast<int64_t>(row) * p.hd) + c8);
+        }
+        __syncthreads();
+        // Tasks: (sequence, 16 query vectors m, 8 columns j of r).  Vector m = row * nq + h
+        // (Q's own row order); D[m][j] = sum_d Q[m][d] P[d][j] in fp32, rounded to bf16 once,
+        // then stored where the scoring loop expects Qp[v][j] of kv head h / g, v = row * g +
+        // h % g: fragment (c, k-step, n-tile v / 8), lane (v % 8) * 4 + t, word half h2, with
+        // (k-step, t, h2) the inverse of frag_r_offset.
+        const int mtiles = (M + 15) >> 4;
+        const int ntp = p.r >> 3;
+        const int ntask = p.num_seqs * mtiles * ntp;
+        uint32_t* cache_words = reinterpret_cast<uint32_t*>(smem_dec);
+        for (int task = warp; task < ntask; task += static_cast<int>(blockDim.x >> 5)) {
+            const int np = task % ntp;
+            const int mt = (task / ntp) % mtiles;
+            const int sq = task / (ntp * mtiles);
+            const int m0 = 16 * mt + gq, m1 = m0 + 8;
+            const uint16_t* q0 = qs + (sq * M + m0) * qstride + 8 * tq;
+            const uint16_t* q1 = q0 + 8 * qstride;
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int l = 0; l < lchunks; ++l) {
+                const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+                const uint4 x0 = m0 < M ? *reinterpret_cast<const uint4*>(q0 + 32 * l) : zero;
+                const uint4 x1 = m1 < M ? *reinterpret_cast<const uint4*>(q1 + 32 * l) : zero;
+                const uint4 b = pfrag[(np * lchunks + l) * 32 + lane];
+                mma_bf16_16816(d, x0.x, x1.x, x0.y, x1.y, b.x, b.y);
+                mma_bf16_16816(d, x0.z, x1.z, x0.w, x1.w, b.z, b.w);
+            }
+            const int j0 = 8 * np + 2 * tq;  // this lane's columns j0, j0 + 1
+            int ks, t2;
+            if constexpr (KSTEPS == 1) {
+                ks = 0;
+                t2 = j0 >> 2;
+            } else {
+                ks = 2 * (j0 >> 5) + ((j0 & 7) >> 2);
+                t2 = (j0 & 31) >> 3;
+            }
+            const int h2 = (j0 & 3) >> 1;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int m = hh ? m1 : m0;
+                if (m < M) {
+                    const int row = m / p.nq;
+                    const int h = m - row * p.nq;
+                    const int c = h / p.g;
+                    const int v = row * p.g + (h - c * p.g);
+                    const int frag = ((sq * p.nkv + c) * KSTEPS + ks) * NT + (v >> 3);
+                    cache_words[(frag * 32 + (v & 7) * 4 + t2) * 2 + h2] =
+                        pack_bf16x2(d[2 * hh], d[2 * hh + 1]);
+                }
+            }
+        }
+        __syncthreads();
+    }
     if (has_work) {
     if (!p.early) {
         s = find_seq(i_begin);
@@ -224,13 +342,20 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
                 }
                 continue;
             }
+            if (!waited && __any_sync(0xffffffffu, my_new == id)) {
+                grid_dependency_wait();  // the slot is being written by the previous kernel
+                waited = true;
+            }
             const uint16_t* slot = p.A_g + (p.layer_slots + id) * slot_elems;
             float best = -INFINITY;
             for (int tb = 0; tb < num_tiles; tb += kTilesPerBatch) {
                 // Issue every load of the batch first (the first one may already be in flight).
                 if (!(preloaded && i == i_begin && tb == 0)) issue_loads(slot, tb);
                 // (Re)fill the query-vector fragment cache while the loads are in flight.
-                if (s != cached_seq) {
+                if (INLINE && s != cached_seq) {
+                    cache = frag_cache_all + s * frag_per_warp;  // the CTA's projection
+                    cached_seq = s;
+                } else if (s != cached_seq) {
                     __syncwarp();
                     for (int c = 0; c < p.nkv; ++c) {
 #pragma unroll
@@ -379,8 +504,9 @@ template <int KSTEPS, int NT>
 hss_status launch_t(const DecodeParams& p, int warps_per_cta, int smem, int grid,
                     cudaStream_t stream) {
     const bool masked = p.ctx_len != nullptr || p.row_pos0 != nullptr;
-    auto k = masked ? score_decode_kernel<KSTEPS, NT, true>
-                    : score_decode_kernel<KSTEPS, NT, false>;
+    auto k = p.Q != nullptr ? score_decode_kernel<KSTEPS, NT, false, true>
+             : masked       ? score_decode_kernel<KSTEPS, NT, true, false>
+                            : score_decode_kernel<KSTEPS, NT, false, false>;
     if (smem > 48 * 1024) {
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
             cudaSuccess)
@@ -398,6 +524,14 @@ int frag_bytes_per_warp(const ScoreArgs& a) {
     return a.num_kv_heads * ksteps * nt * 32 * 8;
 }
 
+// Shared memory of the in-kernel query projection: every sequence's fragment cache, P's
+// fragments, then the query rows.
+int64_t inline_bytes(const ScoreArgs& a, int32_t head_dim) {
+    const int64_t q_rows = static_cast<int64_t>(a.num_seqs) * a.rows_per_seq * a.num_q_heads;
+    return static_cast<int64_t>(a.num_seqs) * frag_bytes_per_warp(a) +
+           static_cast<int64_t>(a.r) * head_dim * 2 + q_rows * (head_dim + 32) * 2;
+}
+
 }  // namespace
 
 bool score_decode_supported(const ScoreArgs& a) {
@@ -409,8 +543,14 @@ bool score_decode_supported(const ScoreArgs& a) {
     return frag_bytes_per_warp(a) <= kFragBudgetBytes;
 }
 
+bool score_decode_inline_supported(const ScoreArgs& a, int32_t head_dim) {
+    if (!score_decode_supported(a) || a.num_seqs < 1 || a.num_seqs > kInlineMaxSeqs) return false;
+    if (head_dim % 32 != 0 || a.ctx_len != nullptr || a.row_pos0 != nullptr) return false;
+    return inline_bytes(a, head_dim) <= kInlineBudgetBytes;
+}
+
 hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream, const FusedRank* fr,
-                               bool* fused) {
+                               bool* fused, const InlineQ* iq) {
     if (fused != nullptr) *fused = false;
     if (a.total == 0) return HSS_OK;
     const DeviceInfo* dev = current_device_info();
@@ -445,6 +585,11 @@ hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream, const Fu
     p.early = 0;
     p.ctx_len = a.ctx_len;
     p.row_pos0 = a.row_pos0;
+    p.Q = nullptr;
+    p.P = nullptr;
+    p.hd = 0;
+    p.cache_bytes = 0;
+    p.nowait = 0;
     if (fr != nullptr && fr->early && fr->num_new <= 64) {
         p.new_ids = fr->new_ids;
         p.num_new = static_cast<int32_t>(fr->num_new);
@@ -452,8 +597,18 @@ hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream, const Fu
     }
 
     const int fb = frag_bytes_per_warp(a);
-    const int warps_per_cta = std::max(1, std::min(kWarpsMax, kFragBudgetBytes / fb));
+    int warps_per_cta = std::max(1, std::min(kWarpsMax, kFragBudgetBytes / fb));
     int smem = warps_per_cta * fb;
+    if (iq != nullptr) {
+        if (!score_decode_inline_supported(a, iq->head_dim)) return HSS_ERR_UNSUPPORTED_SHAPE;
+        p.Q = iq->Q;
+        p.P = iq->P;
+        p.hd = iq->head_dim;
+        p.cache_bytes = a.num_seqs * fb;
+        p.nowait = iq->nowait && p.early && p.num_new <= 32 ? 1 : 0;
+        warps_per_cta = kWarpsMax;
+        smem = static_cast<int>(inline_bytes(a, iq->head_dim));
+    }
     p.frag_bytes_cta = smem;
     // Enough warps for two CTAs per SM; each warp takes a contiguous run of entries.
     const int64_t target_warps = static_cast<int64_t>(dev->num_sms) * 2 * warps_per_cta;

@@ -179,6 +179,11 @@ def test_layer_step_validation(lib):
     assert status_of(hss.hss_layer_step, *base(num_new=-1)) == hss.HSS_ERR_INVALID_ARGUMENT
     assert status_of(hss.hss_layer_step, *base(d=dims(num_kv_heads=3))) == \
         hss.HSS_ERR_INVALID_DIMS
+    # Qp may be NULL only where the decode scorer projects the queries itself.
+    qnull = lambda **o: [x if i != 7 else None for i, x in enumerate(base(**o))]
+    assert status_of(hss.hss_layer_step, *qnull(S=9)) == hss.HSS_ERR_NULL_POINTER
+    wide = dims(num_q_heads=64, num_kv_heads=2)  # 32 query vectors per kv head: tcgen05 path
+    assert status_of(hss.hss_layer_step, *qnull(d=wide)) == hss.HSS_ERR_NULL_POINTER
 
 
 def test_self_test_validation(lib):

@@ -114,3 +114,56 @@ def test_layer_step_against_oracle():
     s_g = sc.cpu().numpy()
     assert_scores_close(s_g, s_o, t_o)
     assert_victims_match(vic.cpu().numpy(), s_o, t_o, case.seq_offsets.numpy(), 8, gpu_scores=s_g)
+
+
+def inline_vs_oracle(d, x, layer, k):
+    """hss_layer_step with Qp = NULL (queries projected inside the scorer) against the
+    oracle; the new slots must equal the projection kernel's, bit for bit."""
+    A = x["A"].clone()
+    sc = torch.empty(x["total"], dtype=torch.float32, device=DEV)
+    vic = torch.full((x["S"], k), 12345, dtype=torch.int32, device=DEV)
+    nb = hss.hss_layer_step_workspace_bytes(x["S"])
+    ws = torch.zeros(max(nb, 4) // 4, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    hss.hss_layer_step(d, x["P"], x["K_new"], x["new_ids"], x["n_new"], x["Q"], x["rows"], None,
+                       A, layer, x["table"], x["offs"], x["S"], x["total"], sc, k, vic, ws, nb, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert int(ws.abs().sum()) == 0, "the workspace must be left zeroed"
+    A_ref, _, _, _ = separate(d, x, layer, k)
+    assert torch.equal(A.view(torch.int16), A_ref.view(torch.int16))
+    Qp_o = oracle.project_q(bits(x["Q"].cpu()).reshape(-1, d.num_q_heads, d.head_dim),
+                            bits(x["P"].cpu()))
+    Qp_o = Qp_o.reshape(x["S"], x["rows"], d.num_q_heads, d.r)
+    offs = x["offs"].cpu().numpy().astype(np.int64)
+    s_o, t_o, _ = oracle.score_blocks(Qp_o, bits(A_ref.cpu()), layer, x["table"].cpu().numpy(),
+                                      offs)
+    s_g = sc.cpu().numpy()
+    assert_scores_close(s_g, s_o, t_o)
+    assert_victims_match(vic.cpu().numpy(), s_o, t_o, offs, k, gpu_scores=s_g)
+
+
+@pytest.mark.parametrize("shape,lengths,rows,n_new,k", [
+    ((2, 32, 8, 128, 32, 16, 2100), [2048], 1, 1, 256),             # the decode layer
+    ((2, 32, 8, 128, 32, 16, 2100), [2048], 1, 0, 256),             # no new block: full wait
+    ((1, 32, 8, 128, 32, 16, 3000), [1500, 0, 700, 9], 1, 40, 64),  # > 32 new blocks, 4 seqs
+    ((1, 8, 2, 64, 16, 16, 900), [0, 5, 300, 1, 0, 77, 400, 2], 2, 3, 8),  # 8 seqs, r 16
+    ((1, 16, 4, 192, 64, 32, 700), [333], 4, 2, 50),                # nvec 16, r 64, bs 32
+    ((1, 64, 8, 256, 32, 16, 500), [450], 2, 5, 33),                # hd 256, nvec 16 (NT 2)
+    ((1, 40, 8, 128, 128, 16, 300), [257], 1, 1, 16),               # r 128, g 5
+])
+def test_layer_step_inline_query_projection(shape, lengths, rows, n_new, k):
+    d = W.Dims(*shape)
+    x = make(d, lengths, rows, n_new, seed=7 * sum(shape) + rows)
+    inline_vs_oracle(d, x, d.num_layers - 1, k)
+
+
+def test_layer_step_inline_new_block_outside_the_table():
+    # A new block that no table entry names is still written; the scorer waits for the
+    # projection only where it reads a new block.
+    d = W.Dims(1, 32, 8, 128, 32, 16, 600)
+    x = make(d, [500], 1, 2, seed=99)
+    in_table = set(x["table"].tolist())
+    outside = next(b for b in range(d.max_blocks) if b not in in_table)
+    x["new_ids"] = torch.tensor([int(x["table"][7]), outside], dtype=torch.int32, device=DEV)
+    inline_vs_oracle(d, x, 0, 32)
