@@ -64,6 +64,9 @@ def _bind(path: str):
     lib.orc_project_kv_blocks.restype = _i64
     lib.orc_project_kv_blocks.argtypes = [_u16p, _u16p, _i64, _i32p, _i64, _i64, _i64, _int,
                                           _int, _int, _int, _u16p, _int]
+    lib.orc_write_kv_tokens.restype = _i64
+    lib.orc_write_kv_tokens.argtypes = [_u16p, _u16p, _i64p, _i64, _i64, _i64, _int, _int, _int,
+                                        _int, _i64, ctypes.c_void_p, _u16p, _int]
     lib.orc_score_blocks.restype = _i64
     lib.orc_score_blocks.argtypes = [_u16p, _i64, _int, _int, _int, _int, _int, _u16p, _i64,
                                      _i64, _i32p, _i64p, _f64p, _f64p, _int]
@@ -162,6 +165,33 @@ def project_kv_blocks(P: np.ndarray, K: np.ndarray, layer: int, block_ids: np.nd
         raise ValueError("inconsistent shapes")
     return int(L.orc_project_kv_blocks(P.reshape(-1), K.reshape(-1), layer, ids, n, nl, mb, nkv,
                                        bs, hd, r, A_g.reshape(-1), nthreads))
+
+
+def write_kv_tokens(P: np.ndarray, K_tok: np.ndarray, slots: np.ndarray, layer: int,
+                    A_g: np.ndarray, K_cache=None, nthreads: int = 1, L=None) -> int:
+    """Token-granular ingest: copy each new token's keys into the paged cache (if given) and
+    write bf16(K . P) into its A_g row, both in place.
+
+    K_tok is [n, num_kv_heads, head_dim]; slots [n] int64 (block * block_size + position,
+    negative = padding); K_cache [max_blocks, block_size, num_kv_heads, head_dim] or None;
+    A_g as in project_kv_blocks.  Returns 0, -1 (bad layer) or i+1 (first slot past the end).
+    """
+    L = L or lib()
+    P = _u16(P)
+    K = _u16(K_tok)
+    for a in (A_g,) + ((K_cache,) if K_cache is not None else ()):
+        if not a.flags.c_contiguous or a.dtype != np.uint16:
+            raise TypeError("A_g and K_cache must be C-contiguous uint16 arrays")
+    sl = np.ascontiguousarray(slots, dtype=np.int64)
+    nl, mb, nkv, bs, r = A_g.shape
+    n, knkv, hd = K.shape
+    if knkv != nkv or P.shape != (hd, r) or sl.shape != (n,):
+        raise ValueError("inconsistent shapes")
+    if K_cache is not None and K_cache.shape != (mb, bs, nkv, hd):
+        raise ValueError("K_cache shape")
+    cache_ptr = None if K_cache is None else K_cache.ctypes.data_as(ctypes.c_void_p)
+    return int(L.orc_write_kv_tokens(P.reshape(-1), K.reshape(-1), sl, n, nl, mb, nkv, bs, hd, r,
+                                     layer, cache_ptr, A_g.reshape(-1), nthreads))
 
 
 def score_blocks(Qp: np.ndarray, A_g: np.ndarray, layer: int, block_table: np.ndarray,

@@ -259,6 +259,76 @@ int64_t orc_project_kv_blocks(const uint16_t* P, const uint16_t* K, int64_t laye
     return 0;
 }
 
+/*
+ * Step 2, token by token, at cache-write time (the page's per-block ingest loop,
+ * Predictor::project_kv_block_on_stream, moved to where new keys are written).
+ *
+ * K_tok   : [n, num_kv_heads, head_dim] bf16, the layer's keys of n new tokens;
+ * slots   : token i goes to block s / block_size, position s % block_size, where
+ *           s = slots[i]; a negative slot marks a padding token (nothing written);
+ * K_cache : [max_blocks, block_size, num_kv_heads, head_dim] bf16 or NULL; gets
+ *           K_cache[blk][t][h][:] = K_tok[i][h][:] (a copy);
+ * A_g     : gets A_g[layer][blk][h][t][j] = bf16( sum_d K_tok[i][h][d] * P[d][j] ).
+ * Returns 0, or the 1-based position of the first token whose slot is at or
+ * past max_blocks * block_size (skipped), or -1 if layer is out of range.
+ */
+typedef struct {
+    const uint16_t* P;
+    const uint16_t* K;
+    const int64_t* slots;
+    uint16_t* cache;
+    uint16_t* A;
+    int64_t layer, max_blocks;
+    int nkv, bs, hd, r;
+} orc_tok_ctx;
+
+static void orc_tok_item(void* c, int64_t i)
+{
+    orc_tok_ctx* k = (orc_tok_ctx*)c;
+    int64_t s = k->slots[i];
+    if (s < 0 || s >= k->max_blocks * k->bs) {
+        return;
+    }
+    int64_t blk = s / k->bs;
+    int t = (int)(s % k->bs);
+    for (int h = 0; h < k->nkv; ++h) {
+        const uint16_t* krow = k->K + (i * k->nkv + h) * (int64_t)k->hd;
+        if (k->cache != NULL) {
+            uint16_t* crow = k->cache + ((blk * k->bs + t) * k->nkv + h) * (int64_t)k->hd;
+            memcpy(crow, krow, (size_t)k->hd * sizeof(uint16_t));
+        }
+        uint16_t* arow = k->A + (((k->layer * k->max_blocks + blk) * k->nkv + h) * k->bs + t) *
+                                    (int64_t)k->r;
+        for (int j = 0; j < k->r; ++j) {
+            double acc = 0.0;
+            for (int d = 0; d < k->hd; ++d) {
+                acc += orc_bf16_to_double(krow[d]) *
+                       orc_bf16_to_double(k->P[(int64_t)d * k->r + j]);
+            }
+            arow[j] = orc_bf16_from_double(acc);
+        }
+    }
+}
+
+int64_t orc_write_kv_tokens(const uint16_t* P, const uint16_t* K_tok, const int64_t* slots,
+                            int64_t n, int64_t num_layers, int64_t max_blocks, int num_kv_heads,
+                            int block_size, int head_dim, int r, int64_t layer,
+                            uint16_t* K_cache, uint16_t* A_g, int nthreads)
+{
+    if (layer < 0 || layer >= num_layers) {
+        return -1;
+    }
+    orc_tok_ctx k = {P, K_tok, slots, K_cache, A_g, layer, max_blocks, num_kv_heads,
+                     block_size, head_dim, r};
+    orc_parallel_for(n, nthreads, orc_tok_item, &k);
+    for (int64_t i = 0; i < n; ++i) {
+        if (slots[i] >= max_blocks * block_size) {
+            return i + 1;
+        }
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Step 3: block scores (Predictor::score_blocks_on_stream)                  */
 /* ------------------------------------------------------------------------ */

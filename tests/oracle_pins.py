@@ -403,6 +403,102 @@ def pin_masked_hand_case(L):
     assert sc.tolist() == [7.0, 3.0], sc     # table order decides positions
 
 
+# ----------------------------------------------------------------------------- token ingest
+
+def _token_case(rng, *, nkv=3, hd=48, bs=4, pool=4, layers=2):
+    """Fresh keys for every position of every block, in a shuffled token order with two
+    padding tokens (slot -1) mixed in.  The token pins keep pool == block_size, so that an
+    oracle that swapped block and position would still index inside its arrays (and fail an
+    assertion instead of writing out of bounds)."""
+    order = rng.permutation(pool * bs)
+    slots = np.concatenate([order, [-1, -1]]).astype(np.int64)
+    rng.shuffle(slots)
+    K_tok = to_bf16_bits(rng.standard_normal((slots.size, nkv, hd)))
+    return K_tok, slots
+
+
+def pin_tokens_identity_brute_force(L):
+    """P = I: every token's A_g row is its key row and its cache row a copy, at the position
+    its slot names; padding writes nothing; other layers stay untouched."""
+    rng = np.random.default_rng(41)
+    nkv, hd, bs, pool, layers, layer = 3, 48, 4, 4, 3, 1
+    K_tok, slots = _token_case(rng, nkv=nkv, hd=hd, bs=bs, pool=pool, layers=layers)
+    P = to_bf16_bits(np.eye(hd))
+    A = np.full((layers, pool, nkv, bs, hd), 0x7FC1, dtype=np.uint16)
+    C = np.full((pool, bs, nkv, hd), 0x7FC1, dtype=np.uint16)
+    assert oracle.write_kv_tokens(P, K_tok, slots, layer, A, K_cache=C, L=L) == 0
+    for i, sl in enumerate(slots):
+        if sl < 0:
+            continue
+        blk, t = divmod(int(sl), bs)
+        assert np.array_equal(C[blk, t], K_tok[i]), "cache row is not the key row"
+        assert np.array_equal(A[layer, blk, :, t], K_tok[i]), "A_g row is not K . I"
+    assert (A[0] == 0x7FC1).all() and (A[2] == 0x7FC1).all(), "wrote another layer"
+
+
+def pin_tokens_selection_projection(L):
+    """P selects r coordinates, times 2: A_g rows are exact numpy slices of the keys."""
+    rng = np.random.default_rng(43)
+    nkv, hd, r, bs, pool = 2, 64, 16, 8, 8
+    K_tok, slots = _token_case(rng, nkv=nkv, hd=hd, bs=bs, pool=pool)
+    sel = rng.permutation(hd)[:r]
+    Pf = np.zeros((hd, r))
+    Pf[sel, np.arange(r)] = 2.0
+    A = np.zeros((1, pool, nkv, bs, r), dtype=np.uint16)
+    assert oracle.write_kv_tokens(to_bf16_bits(Pf), K_tok, slots, 0, A, L=L) == 0
+    Kf = from_bf16_bits(K_tok)
+    for i, sl in enumerate(slots):
+        if sl >= 0:
+            blk, t = divmod(int(sl), bs)
+            assert np.array_equal(from_bf16_bits(A[0, blk, :, t]), 2.0 * Kf[i][:, sel])
+
+
+def pin_tokens_equal_block_projection(L):
+    """Writing a block's tokens one slot at a time (any order, general P) gives the slot the
+    block projection gives; a block written only in part changes only those rows."""
+    rng = np.random.default_rng(47)
+    nkv, hd, r, bs, pool = 2, 64, 16, 4, 4
+    P = to_bf16_bits(rng.standard_normal((hd, r)) / math.sqrt(r))
+    Kb = to_bf16_bits(rng.standard_normal((pool, bs, nkv, hd)))
+    ids = rng.permutation(pool).astype(np.int32)
+    A_blk = np.zeros((1, pool, nkv, bs, r), dtype=np.uint16)
+    assert oracle.project_kv_blocks(P, Kb[ids], 0, ids, A_blk, L=L) == 0
+    A_tok = np.zeros_like(A_blk)
+    order = rng.permutation(pool * bs)
+    slots = order.astype(np.int64)
+    K_tok = Kb.reshape(pool * bs, nkv, hd)[order]
+    assert oracle.write_kv_tokens(P, K_tok, slots, 0, A_tok, L=L) == 0
+    assert np.array_equal(A_tok, A_blk)
+    part = np.full_like(A_blk, 0x7FC1)
+    assert oracle.write_kv_tokens(P, K_tok[:3], slots[:3], 0, part, L=L) == 0
+    written = np.zeros((pool, bs), dtype=bool)
+    for sl in slots[:3]:
+        written[divmod(int(sl), bs)] = True
+    for blk in range(pool):
+        for t in range(bs):
+            row = part[0, blk, :, t]
+            if written[blk, t]:
+                assert np.array_equal(row, A_blk[0, blk, :, t])
+            else:
+                assert (row == 0x7FC1).all()
+
+
+def pin_tokens_out_of_range(L):
+    """A slot past the last block is skipped and reported (1-based position); a bad layer
+    writes nothing."""
+    rng = np.random.default_rng(53)
+    nkv, hd, r, bs, pool = 2, 64, 16, 4, 4
+    P = to_bf16_bits(rng.standard_normal((hd, r)))
+    K_tok = to_bf16_bits(rng.standard_normal((3, nkv, hd)))
+    A = np.zeros((1, pool, nkv, bs, r), dtype=np.uint16)
+    st = oracle.write_kv_tokens(P, K_tok, np.array([5, pool * bs, -1]), 0, A, L=L)
+    assert st == 2
+    assert A[0, 1, :, 1].any() and np.count_nonzero(A.reshape(-1, r).any(axis=1)) == nkv
+    B = np.zeros_like(A)
+    assert oracle.write_kv_tokens(P, K_tok, np.array([0, 1, 2]), 1, B, L=L) == -1
+    assert not B.any()
+
+
 ALL_PINS = [
     pin_bf16_hand_values,
     pin_bf16_matches_torch,
@@ -418,4 +514,8 @@ ALL_PINS = [
     pin_masked_brute_force,
     pin_masked_reduces_to_unmasked,
     pin_masked_hand_case,
+    pin_tokens_identity_brute_force,
+    pin_tokens_selection_projection,
+    pin_tokens_equal_block_projection,
+    pin_tokens_out_of_range,
 ]

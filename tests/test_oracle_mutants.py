@@ -65,6 +65,19 @@ MUTANTS = [
      "if (row_pos0 != NULL && pos > row_pos0[s]) {", 0),
     ("position_not_per_sequence", "i - k->seq_offsets[s], k->ctx_len",
      "i, k->ctx_len", 0),
+    ("token_block_and_position_swapped", "int64_t blk = s / k->bs;\n    int t = (int)(s % k->bs);",
+     "int64_t blk = s % k->bs;\n    int t = (int)(s / k->bs);", 0),
+    ("token_cache_head_major", "((blk * k->bs + t) * k->nkv + h) * (int64_t)k->hd",
+     "((blk * k->nkv + h) * k->bs + t) * (int64_t)k->hd", 0),
+    ("token_a_g_token_major", "((k->layer * k->max_blocks + blk) * k->nkv + h) * k->bs + t)",
+     "((k->layer * k->max_blocks + blk) * k->bs + t) * k->nkv + h)", 0),
+    ("token_ignores_layer", "(((k->layer * k->max_blocks + blk) * k->nkv",
+     "(((0 * k->max_blocks + blk) * k->nkv", 0),
+    ("token_drops_last_term", "for (int d = 0; d < k->hd; ++d) {\n                acc +=",
+     "for (int d = 0; d + 1 < k->hd; ++d) {\n                acc +=", 0),
+    ("token_transposed_P", "k->P[(int64_t)d * k->r + j]", "k->P[(int64_t)j * k->hd + d]", 2),
+    ("token_status_counts_padding", "if (slots[i] >= max_blocks * block_size) {",
+     "if (slots[i] < 0 || slots[i] >= max_blocks * block_size) {", 0),
 ]
 
 
