@@ -39,7 +39,8 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["hss", "reference"], default="hss")
-    p.add_argument("--workload", choices=["decode", "batched", "prefill", "ingest"],
+    p.add_argument("--workload", choices=["decode", "batched", "prefill", "ingest",
+                                          "ingest_tokens"],
                    default="decode")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=200)
@@ -185,10 +186,13 @@ def measured_peaks():
 # dram__bytes_write.sum) from the ncu captures summarised in profiles/, or None when the
 # kernel has changed since its capture.
 TRAFFIC = {
-    "decode": (16865792 + 0, "profiles/score_decode_layer_step.md"),
-    "batched": (283585024 + 2935808, "profiles/score_decode_batched.md"),
-    "prefill": (None, "profiles/score_tc_prefill.md: kernel changed since the capture"),
-    "ingest": (None, "profiles/project_ingest_40000_blocks.md: kernel changed since the capture"),
+    "decode": (16853504 + 0, "profiles/score_decode_plain.md"),
+    "batched": (283584000 + 3072512, "profiles/score_decode_batched.md"),
+    "prefill": (140040192 + 3555584, "profiles/score_tc_prefill.md"),
+    # captured on a 40000-block launch; traffic grows with the blocks, so scaled to 4096
+    "ingest": (round((1310970000 + 305094400) * 4096 / 40000),
+               "profiles/project_ingest_40000_blocks.md, scaled from 40000 to 4096 blocks"),
+    "ingest_tokens": (None, "no capture of the token path yet"),
 }
 
 
@@ -600,8 +604,77 @@ class IngestWorkload(_Base):
         return sum(k.numel() for k in self.K) * 2 + self.Q.numel() * 2, self.k * 4
 
 
+class IngestTokensWorkload(IngestWorkload):
+    """The ingest workload through the cache-write path: each layer's keys of the 4096 new
+    blocks arrive as 65536 tokens (block * 16 + position slots) and one hss_write_kv_tokens
+    call per layer writes them into the paged key cache and their projections into A_g."""
+
+    name = "ingest_tokens"
+
+    def __init__(self, device, seed: int):
+        super().__init__(device, seed)
+        torch, d = self.torch, self.dims
+        bs, nkv, hd = d.block_size, d.num_kv_heads, d.head_dim
+        ids = self.new_ids.to(torch.int64)
+        self.slots = (ids[:, None] * bs + torch.arange(bs, device=device)[None, :]).reshape(-1)
+        self.n_tok = self.slots.numel()
+        self.K_tok = [k.view(self.n_tok, nkv, hd) for k in self.K]
+        # One paged key cache (2 GiB) that every layer writes: the same bytes per call as a
+        # cache per layer.
+        self.cache = torch.empty(d.max_blocks, bs, nkv, hd, dtype=torch.bfloat16, device=device)
+        torch.cuda.synchronize()
+
+    def ingest(self, l):
+        self.hss.hss_write_kv_tokens(self.dims, self.P, self.K_tok[l], self.slots, self.n_tok,
+                                     self.cache, self.A, l)
+
+    def step(self):
+        hss, d = self.hss, self.dims
+        for l in range(self.L):
+            self.ingest(l)
+        hss.hss_project_q(d, self.P, self.Q, 1, self.Qp)
+        hss.hss_score_blocks(d, self.Qp, 1, self.A, self.layer, self.table, self.offs, 1, self.n,
+                             self.scores)
+        hss.hss_rank_victims(self.scores, self.offs, 1, self.n, self.k, self.victims)
+
+    dominant_kernel = "project (cache write + A_g, tokens)"
+
+    @property
+    def dominant_units(self):
+        d = self.dims
+        # key row read, key row written to the cache, A_g row written; P once; slots
+        return (self.n_tok * d.num_kv_heads * (2 * d.head_dim * 2 + d.r * 2) +
+                d.head_dim * d.r * 2 + self.n_tok * 8)
+
+    def dominant(self):
+        for l in range(self.L):
+            self.ingest(l)
+
+    def describe(self):
+        return (f"ingest + score under skew through the cache write: {self.n_tok} new tokens "
+                f"({self.new_ids.numel()} blocks) written into the paged key cache and A_g of "
+                f"each of {self.L} layers (one call per layer), then layer {self.layer}'s "
+                f"{self.n} blocks scored, bottom-{self.k}")
+
+    l2_note = ("no flush: each step reads 4 GiB of keys and writes 4 GiB of cache and 1 GiB of "
+               "A_g, far above the 129 MB L2")
+
+    def e2e_step(self):
+        hss, d = self.hss, self.dims
+        for l in range(self.L):
+            self.K[l].copy_(self.h_K[l], non_blocking=True)
+            self.ingest(l)
+        self.Q.copy_(self.h_Q, non_blocking=True)
+        hss.hss_project_q(d, self.P, self.Q, 1, self.Qp)
+        hss.hss_score_blocks(d, self.Qp, 1, self.A, self.layer, self.table, self.offs, 1, self.n,
+                             self.scores)
+        hss.hss_rank_victims(self.scores, self.offs, 1, self.n, self.k, self.victims)
+        self.h_vic.copy_(self.victims, non_blocking=True)
+        self.torch.cuda.current_stream().synchronize()
+
+
 WORKLOADS = {"decode": DecodeWorkload, "batched": BatchedWorkload, "prefill": PrefillWorkload,
-             "ingest": IngestWorkload}
+             "ingest": IngestWorkload, "ingest_tokens": IngestTokensWorkload}
 
 
 # ----------------------------------------------------------------------------- oracle timing
@@ -613,7 +686,8 @@ def _bits(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-SAMPLE_BLOCKS = {"decode": 2048, "batched": 544, "prefill": 8, "ingest": 256}
+SAMPLE_BLOCKS = {"decode": 2048, "batched": 544, "prefill": 8, "ingest": 256,
+                 "ingest_tokens": 256}
 
 
 class OracleSample:
@@ -631,13 +705,17 @@ class OracleSample:
         import workloads as W
 
         self.np, self.oracle, self.threads = np, oracle, threads
-        one = lambda d: W.Dims(1, d.num_q_heads, d.num_kv_heads, d.head_dim, d.r, d.block_size,
-                               d.max_blocks)
+        self.tokens = name == "ingest_tokens"  # ingest through the oracle's cache write
+        if self.tokens:
+            name = "ingest"
+        one = lambda d, mb=None: W.Dims(1, d.num_q_heads, d.num_kv_heads, d.head_dim, d.r,
+                                        d.block_size, mb or d.max_blocks)
         # (dims, query rows, key distribution, blocks drawn, ingest per call, ingest per scored)
         spec = {"decode": (one(W.DECODE), 1, "normal", 2048, 1, 0.0),
                 "batched": (W.BATCHED, 1, "normal", 1024, 0, 0.0),
                 "prefill": (W.PREFILL, 512, "normal", 64, 32, 0.0),
-                "ingest": (one(W.INGEST), 1, "skewed", 1024, 0, 2.0)}[name]
+                "ingest": (one(W.INGEST, 1024 if self.tokens else None), 1, "skewed", 1024, 0,
+                           2.0)}[name]
         dims, rows, kind, pool, self.extra_ingest, self.ingest_ratio = spec
         m = SAMPLE_BLOCKS[name]
         c = W.generic(name, dims, num_seqs=1, rows_per_seq=rows, lengths=[min(m, pool)],
@@ -652,6 +730,9 @@ class OracleSample:
         self.table = c.table.numpy()
         self.pool = self.K.shape[0]
         self.A = np.zeros((1, d.max_blocks, d.num_kv_heads, d.block_size, d.r), dtype=np.uint16)
+        if self.tokens:
+            self.cache = np.zeros((d.max_blocks, d.block_size, d.num_kv_heads, d.head_dim),
+                                  dtype=np.uint16)
 
     def call(self, m: int):
         """One sampled call scoring m entries; returns m."""
@@ -660,8 +741,18 @@ class OracleSample:
         n_ing = self.extra_ingest + int(round(self.ingest_ratio * m))
         if n_ing > 0:
             pos = np.arange(n_ing) % self.pool
-            oracle.project_kv_blocks(self.P, self.K[pos], 0, ids[pos % m] if m else pos.astype(
-                np.int32), self.A, nthreads=self.threads)
+            bid = ids[pos % m] if m else pos.astype(np.int32)
+            if self.tokens:
+                d = c.dims
+                slots = (bid.astype(np.int64)[:, None] * d.block_size +
+                         np.arange(d.block_size)[None, :]).reshape(-1)
+                oracle.write_kv_tokens(self.P, self.K[pos].reshape(-1, d.num_kv_heads,
+                                                                   d.head_dim),
+                                       slots, 0, self.A, K_cache=self.cache,
+                                       nthreads=self.threads)
+            else:
+                oracle.project_kv_blocks(self.P, self.K[pos], 0, bid, self.A,
+                                         nthreads=self.threads)
         Qp = oracle.project_q(self.Q, self.P, nthreads=self.threads)
         offs = np.array([0, m], dtype=np.int64)
         s, _, _ = oracle.score_blocks(Qp, self.A, 0, ids, offs, nthreads=self.threads)

@@ -121,6 +121,32 @@ hss_status hss_project_kv_blocks(const hss_dims* dims, const uint16_t* P, const 
                                  int32_t layer, const int32_t* block_ids, int64_t num_blocks,
                                  uint16_t* A_g, int32_t* dev_status, void* stream);
 
+/*
+ * Cache write with projection: the page's ingest (Predictor::project_kv_block, launched once
+ * per block after a block is written) moved to where the layer's new keys are written, one
+ * token at a time.  For every token i with slot s = slots[i] = block * block_size + t:
+ *   K_cache[s / block_size][s % block_size][h][:] = K_tok[i][h][:]        (if K_cache != NULL)
+ *   A_g[layer][s / block_size][h][s % block_size][:] = bf16(K_tok[i][h] . P)
+ * for every kv head h, in one launch.  A decode step (one new token per sequence) thus keeps
+ * A_g current without waiting for a block to fill; the rows of positions not yet written
+ * keep what they held (score such blocks with a ctx_len mask, hss_score_blocks_masked).
+ *   K_tok    device, [num_tokens, num_kv_heads, head_dim] bf16, 16-byte aligned: the layer's
+ *            keys of the new tokens
+ *   slots    device, [num_tokens] int64, 8-byte aligned.  A negative slot marks a padding
+ *            token: nothing is written for it.  A slot >= max_blocks * block_size is skipped
+ *            and raises HSS_ERR_OUT_OF_RANGE in *dev_status (if not NULL) and the library's
+ *            device error word.  If two tokens name one slot, either may win.
+ *   K_cache  device, [max_blocks, block_size, num_kv_heads, head_dim] bf16, 16-byte aligned:
+ *            this layer's paged key cache (each block in the page's k_block layout), or NULL
+ *            to write A_g only
+ *   A_g      as in hss_project_kv_blocks
+ * Each A_g row equals what hss_project_kv_blocks writes for that position (the same kernel
+ * computes it).  Errors as hss_project_kv_blocks.
+ */
+hss_status hss_write_kv_tokens(const hss_dims* dims, const uint16_t* P, const uint16_t* K_tok,
+                               const int64_t* slots, int64_t num_tokens, uint16_t* K_cache,
+                               uint16_t* A_g, int32_t layer, int32_t* dev_status, void* stream);
+
 /* Score kernel choice for hss_score_blocks. */
 #define HSS_PATH_AUTO 0    /* decode kernel when rows_per_seq * (num_q_heads/num_kv_heads) <= 16,
                               else the tensor-memory (tcgen05) kernel */

@@ -41,7 +41,7 @@ EXPORTED = (
     "hss_project_kv_blocks", "hss_score_blocks", "hss_rank_victims", "hss_read_device_error",
     "hss_layer_step", "hss_layer_step_workspace_bytes", "hss_layer_step_static",
     "hss_score_blocks_masked",
-    "hss_layer_step_static_max_seqs", "hss_self_test_wait_timeout",
+    "hss_layer_step_static_max_seqs", "hss_write_kv_tokens", "hss_self_test_wait_timeout",
 )
 
 
@@ -100,6 +100,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.hss_project_q.argtypes = [dp, vp, vp, i64, vp, vp]
     lib.hss_project_kv_blocks.restype = i32
     lib.hss_project_kv_blocks.argtypes = [dp, vp, vp, i32, vp, i64, vp, vp, vp]
+    lib.hss_write_kv_tokens.restype = i32
+    lib.hss_write_kv_tokens.argtypes = [dp, vp, vp, vp, i64, vp, vp, i32, vp, vp]
     lib.hss_score_blocks.restype = i32
     lib.hss_score_blocks.argtypes = [dp, vp, i32, vp, i32, vp, vp, i32, i64, vp, i32, vp, vp]
     lib.hss_score_blocks_masked.restype = i32
@@ -182,6 +184,16 @@ def hss_project_kv_blocks(dims, P, K, layer: int, block_ids, num_blocks: int, A_
                                       int(layer), _ptr(block_ids), int(num_blocks), _ptr(A_g),
                                       _ptr(dev_status), _stream(stream))
     _check(st, "hss_project_kv_blocks")
+
+
+def hss_write_kv_tokens(dims, P, K_tok, slots, num_tokens: int, K_cache, A_g, layer: int,
+                        dev_status=None, stream=None) -> None:
+    """K_cache[slot] = K_tok[i] and A_g[layer][slot's block][h][slot's position] =
+    bf16(K_tok[i][h] . P) for every new token i (K_cache may be None)."""
+    st = load().hss_write_kv_tokens(ctypes.byref(hss_dims.of(dims)), _ptr(P), _ptr(K_tok),
+                                    _ptr(slots), int(num_tokens), _ptr(K_cache), _ptr(A_g),
+                                    int(layer), _ptr(dev_status), _stream(stream))
+    _check(st, "hss_write_kv_tokens")
 
 
 def hss_score_blocks(dims, Qp, rows_per_seq: int, A_g, layer: int, block_table, seq_offsets,

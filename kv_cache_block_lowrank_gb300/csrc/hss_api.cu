@@ -141,6 +141,37 @@ hss_status hss_project_kv_blocks(const hss_dims* dims, const uint16_t* P, const 
     return launch_project(a, static_cast<cudaStream_t>(stream));
 }
 
+hss_status hss_write_kv_tokens(const hss_dims* dims, const uint16_t* P, const uint16_t* K_tok,
+                               const int64_t* slots, int64_t num_tokens, uint16_t* K_cache,
+                               uint16_t* A_g, int32_t layer, int32_t* dev_status, void* stream) {
+    hss_status st = check_dims(dims);
+    if (st != HSS_OK) return st;
+    if (layer < 0 || layer >= dims->num_layers) return HSS_ERR_OUT_OF_RANGE;
+    if (num_tokens < 0) return HSS_ERR_INVALID_ARGUMENT;
+    if (num_tokens == 0) return HSS_OK;
+    if (P == nullptr || K_tok == nullptr || slots == nullptr || A_g == nullptr)
+        return HSS_ERR_NULL_POINTER;
+    if (!aligned16(P) || !aligned16(K_tok) || !aligned16(A_g) ||
+        (K_cache != nullptr && !aligned16(K_cache)) || (reinterpret_cast<uintptr_t>(slots) & 7u))
+        return HSS_ERR_MISALIGNED;
+    if (num_tokens > (int64_t{1} << 31) / dims->num_kv_heads) return HSS_ERR_INVALID_ARGUMENT;
+    ProjectArgs a{};
+    a.P = P;
+    a.X = K_tok;
+    a.num_rows = num_tokens * dims->num_kv_heads;
+    a.head_dim = dims->head_dim;
+    a.r = dims->r;
+    a.out = A_g;
+    a.slots = slots;
+    a.cache = K_cache;
+    a.num_kv_heads = dims->num_kv_heads;
+    a.block_size = dims->block_size;
+    a.max_blocks = dims->max_blocks;
+    a.layer = layer;
+    a.dev_status = dev_status;
+    return launch_project(a, static_cast<cudaStream_t>(stream));
+}
+
 hss_status hss_score_blocks(const hss_dims* dims, const uint16_t* Qp, int32_t rows_per_seq,
                             const uint16_t* A_g, int32_t layer, const int32_t* block_table,
                             const int32_t* seq_offsets, int32_t num_seqs, int64_t total_blocks,

@@ -55,8 +55,12 @@ struct ProjectArgs {
     int32_t head_dim;
     int32_t r;
     uint16_t* out;
-    // A_g mode only
+    // A_g modes: block_ids (whole blocks, rows in the page's k_block order) or slots (one
+    // row per (token, kv head): token i goes to slot slots[i] = block * block_size + t,
+    // negative = padding; cache, if not null, gets a copy of the key row at that slot)
     const int32_t* block_ids;
+    const int64_t* slots;
+    uint16_t* cache;
     int32_t num_kv_heads;
     int32_t block_size;
     int64_t max_blocks;

@@ -66,7 +66,10 @@ struct ProjSegment {
     int64_t num_rows;
     int64_t tiles;             // ceil(num_rows / 128)
     uint16_t* out;
-    const int32_t* block_ids;  // nullptr: rows go to out + m * r (Qp); else A_g slot rows
+    const int32_t* block_ids;  // whole blocks -> A_g slot rows
+    const int64_t* slots;      // single tokens -> A_g rows (both null: rows go to out + m * r)
+    uint16_t* cache;           // slots mode: the key row is also copied to cache[slot][h]
+    const uint16_t* X;         // the input rows (for that copy)
 };
 
 struct ProjParams {
@@ -261,7 +264,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t m = (second ? tile - p.seg[0].tiles : tile) * kBM + row_in_tile;
             uint16_t* dst = nullptr;
             if (m < sg.num_rows) {
-                if (sg.block_ids == nullptr) {
+                if (sg.slots != nullptr) {
+                    // Row m = (token i, kv head h); the token's slot names block and position.
+                    const int64_t i = m / p.num_kv_heads;
+                    const int h = static_cast<int>(m - i * p.num_kv_heads);
+                    const int64_t sl = sg.slots[i];
+                    if (sl >= 0 && sl < p.max_blocks * p.block_size) {
+                        const int64_t blk = sl / p.block_size;
+                        const int t = static_cast<int>(sl - blk * p.block_size);
+                        dst = sg.out + (((p.layer_slots + blk) * p.num_kv_heads + h) *
+                                            p.block_size + t) * static_cast<int64_t>(r);
+                        if (sg.cache != nullptr) {  // the key row, still in L2, to the cache
+                            const uint4* src =
+                                reinterpret_cast<const uint4*>(sg.X + m * p.head_dim);
+                            uint4* cd = reinterpret_cast<uint4*>(
+                                sg.cache + (sl * p.num_kv_heads + h) * p.head_dim);
+                            for (int c = 0; c < p.head_dim / 8; c += 8) {
+                                uint4 b[8];
+#pragma unroll
+                                for (int u = 0; u < 8; ++u) b[u] = __ldg(src + c + u);
+#pragma unroll
+                                for (int u = 0; u < 8; ++u) cd[c + u] = b[u];
+                            }
+                        }
+                    } else if (sl >= 0 && h == 0) {
+                        raise_error(p.dev_status, p.lib_error, HSS_ERR_OUT_OF_RANGE);
+                    }
+                } else if (sg.block_ids == nullptr) {
                     dst = sg.out + m * r;
                 } else {
                     const int64_t i = m / rows_per_block;
@@ -397,14 +426,17 @@ hss_status launch_project2(const ProjectArgs& a0, const ProjectArgs* a1, cudaStr
     const ProjectArgs* kv = nullptr;
     for (int i = 0; i < 2; ++i) {
         if (segs[i] == nullptr) {
-            p.seg[i] = ProjSegment{0, 0, nullptr, nullptr};
+            p.seg[i] = ProjSegment{0, 0, nullptr, nullptr, nullptr, nullptr, nullptr};
             continue;
         }
         p.seg[i].num_rows = segs[i]->num_rows;
         p.seg[i].tiles = (segs[i]->num_rows + kBM - 1) / kBM;
         p.seg[i].out = segs[i]->out;
         p.seg[i].block_ids = segs[i]->block_ids;
-        if (segs[i]->block_ids != nullptr) kv = segs[i];
+        p.seg[i].slots = segs[i]->slots;
+        p.seg[i].cache = segs[i]->cache;
+        p.seg[i].X = segs[i]->X;
+        if (segs[i]->block_ids != nullptr || segs[i]->slots != nullptr) kv = segs[i];
     }
     p.num_kv_heads = kv != nullptr ? kv->num_kv_heads : 1;
     p.block_size = kv != nullptr ? kv->block_size : 1;
