@@ -67,6 +67,11 @@ def _bind(path: str):
     lib.orc_write_kv_tokens.restype = _i64
     lib.orc_write_kv_tokens.argtypes = [_u16p, _u16p, _i64p, _i64, _i64, _i64, _int, _int, _int,
                                         _int, _i64, ctypes.c_void_p, _u16p, _int]
+    lib.orc_score_rows.restype = _i64
+    lib.orc_score_rows.argtypes = [_u16p, _i64, _int, _int, _int, _int, _u16p, _i64, _i64, _i32p,
+                                   _i64, _f64p, _f64p, _int]
+    lib.orc_select_rows.restype = _int
+    lib.orc_select_rows.argtypes = [_f32p, _i64, _i64, _i64, _i64, _int, _int, _i32p]
     lib.orc_score_blocks.restype = _i64
     lib.orc_score_blocks.argtypes = [_u16p, _i64, _int, _int, _int, _int, _int, _u16p, _i64,
                                      _i64, _i32p, _i64p, _f64p, _f64p, _int]
@@ -192,6 +197,46 @@ def write_kv_tokens(P: np.ndarray, K_tok: np.ndarray, slots: np.ndarray, layer: 
     cache_ptr = None if K_cache is None else K_cache.ctypes.data_as(ctypes.c_void_p)
     return int(L.orc_write_kv_tokens(P.reshape(-1), K.reshape(-1), sl, n, nl, mb, nkv, bs, hd, r,
                                      layer, cache_ptr, A_g.reshape(-1), nthreads))
+
+
+def score_rows(Qp: np.ndarray, A_g: np.ndarray, layer: int, table: np.ndarray,
+               nthreads: int = 1, L=None):
+    """Per-row block scores of one sequence's chunk, in fp64.
+
+    Qp is [rows, num_q_heads, r]; table [n] physical ids.  Returns (score [rows, n] f64,
+    tsum [rows, n] f64, bad_entries).
+    """
+    L = L or lib()
+    Qp = _u16(Qp)
+    if not A_g.flags.c_contiguous or A_g.dtype != np.uint16:
+        raise TypeError("A_g must be a C-contiguous uint16 array")
+    rows, nq, r = Qp.shape
+    nl, mb, nkv, bs, ar = A_g.shape
+    if ar != r:
+        raise ValueError("inconsistent shapes")
+    t = np.ascontiguousarray(table, dtype=np.int32)
+    n = t.size
+    score = np.empty((rows, n), dtype=np.float64)
+    tsum = np.empty((rows, n), dtype=np.float64)
+    bad = L.orc_score_rows(Qp.reshape(-1), rows, nq, nkv, r, bs, A_g.reshape(-1), layer, mb, t, n,
+                           score.reshape(-1), tsum.reshape(-1), nthreads)
+    return score, tsum, int(bad)
+
+
+def select_rows(scores: np.ndarray, n: int, first_pos: int, block_size: int, topk: int,
+                L=None) -> np.ndarray:
+    """Per-row top-k (larger score first, lower index on ties) over the blocks each row has
+    seen whole.  scores is [rows, stride] f32 with stride >= n; returns [rows, topk] int32."""
+    L = L or lib()
+    sc = np.ascontiguousarray(scores, dtype=np.float32)
+    rows, stride = sc.shape
+    if stride < n:
+        raise ValueError("stride < n")
+    out = np.empty((rows, topk), dtype=np.int32)
+    if L.orc_select_rows(sc.reshape(-1), rows, n, stride, first_pos, block_size, topk,
+                         out.reshape(-1)) != 0:
+        raise MemoryError("oracle allocation failed")
+    return out
 
 
 def score_blocks(Qp: np.ndarray, A_g: np.ndarray, layer: int, block_table: np.ndarray,

@@ -668,3 +668,115 @@ int orc_rank_victims(const float* scores, const int64_t* seq_offsets, int64_t nu
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Step 5: per-row scores and per-row selection (QSA-style, page            */
+/* "metrale_model_layers/layers/qsa_select.rs", host top-k per row)          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * One sequence's chunk of query rows, each row on its own:
+ * Qp     : [rows, num_q_heads, r] bf16;
+ * table  : [n] physical block ids of the sequence, in order;
+ * score[row * n + j] : max over query heads h and tokens t of block table[j]
+ *          of sum_k Qp[row][h][k] * A_g[layer][table[j]][h / g][t][k], in fp64
+ *          (the block score of orc_score_blocks, without the max over rows);
+ * tsum   : the largest sum_k |Qp_k * A_k| over the same candidates.
+ * An id outside [0, max_blocks) scores -inf (it is never selected), tsum 0.
+ * Returns the number of such entries.
+ */
+typedef struct {
+    orc_score_shape shape;
+    const int32_t* table;
+    int64_t n;
+    double* score;
+    double* tsum;
+} orc_rows_ctx;
+
+static void orc_rows_item(void* c, int64_t i)
+{
+    orc_rows_ctx* k = (orc_rows_ctx*)c;
+    int64_t row = i / k->n;
+    int64_t j = i - row * k->n;
+    int64_t id = k->table[j];
+    if (id < 0 || id >= k->shape.max_blocks) {
+        k->score[i] = -INFINITY;
+        k->tsum[i] = 0.0;
+        return;
+    }
+    /* A one-row view of the chunk: sequence `row`, one row per sequence. */
+    orc_score_shape one = k->shape;
+    one.rows = 1;
+    orc_score_one(&one, row, id, &k->score[i], &k->tsum[i]);
+}
+
+int64_t orc_score_rows(const uint16_t* Qp, int64_t rows, int num_q_heads, int num_kv_heads,
+                       int r, int block_size, const uint16_t* A_g, int64_t layer,
+                       int64_t max_blocks, const int32_t* table, int64_t n, double* score,
+                       double* tsum, int nthreads)
+{
+    orc_rows_ctx k;
+    k.shape.Qp = Qp;
+    k.shape.A = A_g;
+    k.shape.layer = layer;
+    k.shape.max_blocks = max_blocks;
+    k.shape.rows = 1;
+    k.shape.nq = num_q_heads;
+    k.shape.nkv = num_kv_heads;
+    k.shape.r = r;
+    k.shape.bs = block_size;
+    k.table = table;
+    k.n = n;
+    k.score = score;
+    k.tsum = tsum;
+    orc_parallel_for(rows * n, nthreads, orc_rows_item, &k);
+    int64_t bad = 0;
+    for (int64_t j = 0; j < n; ++j) {
+        if (table[j] < 0 || table[j] >= max_blocks) {
+            ++bad;
+        }
+    }
+    return bad;
+}
+
+/*
+ * scores : [rows, stride] f32; row r's score of block j is scores[r * stride + j];
+ * row r (at position first_pos + r) considers the blocks it has seen whole,
+ *   j < complete_r = min(n, (first_pos + r + 1) / block_size),
+ * orders them by score, larger first, lower index first among equal scores
+ * (-0 equals +0; NaN ranks below every number), and lists the first topk:
+ * lists[r * topk + i], -1 where complete_r <= i.
+ */
+int orc_select_rows(const float* scores, int64_t rows, int64_t n, int64_t stride,
+                    int64_t first_pos, int block_size, int topk, int32_t* lists)
+{
+    orc_keyed* keyed = (orc_keyed*)malloc(sizeof(orc_keyed) * (size_t)(n > 0 ? n : 1));
+    if (keyed == NULL) {
+        return -1;
+    }
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t complete = (first_pos + r + 1) / block_size;
+        if (complete > n) {
+            complete = n;
+        }
+        if (complete < 0) {
+            complete = 0;
+        }
+        for (int64_t j = 0; j < complete; ++j) {
+            double v = (double)scores[r * stride + j];
+            /* ascending order of v = descending order of the score */
+            v = isnan(v) ? INFINITY : -v;
+            if (v == 0.0) {
+                v = 0.0; /* -0 -> +0 */
+            }
+            keyed[j].v = v;
+            keyed[j].idx = (int32_t)j;
+        }
+        qsort(keyed, (size_t)complete, sizeof(orc_keyed), orc_keyed_cmp);
+        for (int i = 0; i < topk; ++i) {
+            lists[r * (int64_t)topk + i] = i < complete ? keyed[i].idx : -1;
+        }
+    }
+    free(keyed);
+    return 0;
+}

@@ -499,6 +499,68 @@ def pin_tokens_out_of_range(L):
     assert not B.any()
 
 
+# ----------------------------------------------------------------------------- per-row selection
+
+def pin_rows_identity_brute_force(L):
+    """P = I: per-row scores are the per-row max of the full Q.K^T (numpy), exactly; their
+    max over rows is the pinned block score; a bad id scores -inf."""
+    rng = np.random.default_rng(61)
+    nq, nkv, hd, bs, R, pool, n = 6, 2, 32, 4, 5, 9, 7
+    P = to_bf16_bits(np.eye(hd))
+    Q = bf16_normal_bits(rng, (R, nq, hd))
+    K = bf16_normal_bits(rng, (pool, bs, nkv, hd))
+    ids = np.arange(pool, dtype=np.int32)
+    A = np.zeros((2, pool, nkv, bs, hd), dtype=np.uint16)
+    assert oracle.project_kv_blocks(P, K, 1, ids, A, L=L) == 0
+    table = rng.permutation(pool)[:n].astype(np.int32)
+    score, tsum, bad = oracle.score_rows(Q, A, 1, table, L=L)
+    assert bad == 0 and score.shape == (R, n)
+    Qf, Kf = from_bf16_bits(Q), from_bf16_bits(K)
+    g = nq // nkv
+    for row in range(R):
+        for j, bid in enumerate(table):
+            exp = max(float((Kf[bid][:, h // g, :] @ Qf[row, h]).max()) for h in range(nq))
+            assert score[row, j] == exp, (row, j)
+    blk, btsum, _ = oracle.score_blocks(Q[None], A, 1, table, np.array([0, n]), L=L)
+    assert np.array_equal(score.max(axis=0), blk)
+    assert np.array_equal(tsum.max(axis=0), btsum)
+    bad_table = table.copy()
+    bad_table[2] = pool + 3
+    sc2, _, bad2 = oracle.score_rows(Q, A, 1, bad_table, L=L)
+    assert bad2 == 1 and np.all(np.isneginf(sc2[:, 2]))
+
+
+def pin_rows_selection_brute_force(L):
+    """Per-row top-k against a plain Python sort (larger first, lower index on ties), over
+    the blocks each row has seen whole, with ties, signed zeros and NaN."""
+    rng = np.random.default_rng(67)
+    rows, n, stride, bs, topk = 9, 13, 16, 4, 5
+    sc = rng.integers(-3, 4, size=(rows, stride)).astype(np.float32)  # many ties
+    sc[1, 2] = -0.0
+    sc[1, 3] = 0.0
+    sc[2, 0] = np.nan
+    sc[3, :] = np.nan
+    for first_pos in (0, 3, 17, 40):
+        got = oracle.select_rows(sc, n, first_pos, bs, topk, L=L)
+        for r in range(rows):
+            complete = min(n, (first_pos + r + 1) // bs)
+            key = lambda j: (-math.inf if math.isnan(sc[r, j]) else float(sc[r, j]) + 0.0, -j)
+            order = sorted(range(complete), key=key, reverse=True)
+            exp = (order + [-1] * topk)[:topk]
+            assert got[r].tolist() == exp, (first_pos, r, got[r].tolist(), exp)
+
+
+def pin_rows_selection_hand_case(L):
+    """Block size 4, three blocks with scores 2, 5, 5 (row 0) and 7, 1, 9 (row 1)."""
+    sc = np.array([[2.0, 5.0, 5.0], [7.0, 1.0, 9.0]], dtype=np.float32)
+    # first_pos 6: row 0 sits at 6 and has seen block 0 whole; row 1 (at 7) blocks 0, 1.
+    assert oracle.select_rows(sc, 3, 6, 4, 2, L=L).tolist() == [[0, -1], [0, 1]]
+    # first_pos 10: row 0 (at 10) sees blocks 0, 1; row 1 (at 11) all three.
+    assert oracle.select_rows(sc, 3, 10, 4, 2, L=L).tolist() == [[1, 0], [2, 0]]
+    # Equal scores: the lower index first.
+    assert oracle.select_rows(sc, 3, 100, 4, 3, L=L).tolist() == [[1, 2, 0], [2, 0, 1]]
+
+
 ALL_PINS = [
     pin_bf16_hand_values,
     pin_bf16_matches_torch,
@@ -518,4 +580,7 @@ ALL_PINS = [
     pin_tokens_selection_projection,
     pin_tokens_equal_block_projection,
     pin_tokens_out_of_range,
+    pin_rows_identity_brute_force,
+    pin_rows_selection_brute_force,
+    pin_rows_selection_hand_case,
 ]

@@ -15,8 +15,10 @@ import oracle_pins as pins
 SRC = open(os.path.join(os.path.dirname(oracle.__file__), "hss_oracle.c")).read()
 
 # (name, text to replace, replacement, which occurrence (0-based)).
-# Not listed: loosening the explicit overflow test in the bf16 rounding, which
-# is an equivalent mutant (the binary32 conversion of 2^128 is +inf anyway).
+# Not listed, because they are equivalent mutants (no input tells them apart):
+# loosening the explicit overflow test in the bf16 rounding (the binary32
+# conversion of 2^128 is +inf anyway), and dropping the -0 -> +0 step of the
+# per-row selection (its comparator already orders -0 and +0 as equal).
 MUTANTS = [
     ("q_drops_first_term", "for (int d = 0; d < k->hd; ++d) {\n            acc +=",
      "for (int d = 1; d < k->hd; ++d) {\n            acc +=", 0),
@@ -76,6 +78,13 @@ MUTANTS = [
     ("token_drops_last_term", "for (int d = 0; d < k->hd; ++d) {\n                acc +=",
      "for (int d = 0; d + 1 < k->hd; ++d) {\n                acc +=", 0),
     ("token_transposed_P", "k->P[(int64_t)d * k->r + j]", "k->P[(int64_t)j * k->hd + d]", 2),
+    ("rows_max_over_all_rows", "    one.rows = 1;\n    orc_score_one(&one, row, id,",
+     "    one.rows = 1;\n    orc_score_one(&one, 0, id,", 0),
+    ("rows_bad_id_plus_inf", "        k->score[i] = -INFINITY;", "        k->score[i] = INFINITY;", 0),
+    ("select_complete_off_by_one", "int64_t complete = (first_pos + r + 1) / block_size;",
+     "int64_t complete = (first_pos + r) / block_size;", 0),
+    ("select_ascending", "v = isnan(v) ? INFINITY : -v;", "v = isnan(v) ? INFINITY : v;", 0),
+    ("select_nan_first", "v = isnan(v) ? INFINITY : -v;", "v = isnan(v) ? -INFINITY : -v;", 0),
     ("token_status_counts_padding", "if (slots[i] >= max_blocks * block_size) {",
      "if (slots[i] < 0 || slots[i] >= max_blocks * block_size) {", 0),
 ]
