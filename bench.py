@@ -40,7 +40,7 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["hss", "reference"], default="hss")
     p.add_argument("--workload", choices=["decode", "batched", "prefill", "ingest",
-                                          "ingest_tokens"],
+                                          "ingest_tokens", "prefill_rows"],
                    default="decode")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=200)
@@ -193,6 +193,7 @@ TRAFFIC = {
     "ingest": (round((1310970000 + 305094400) * 4096 / 40000),
                "profiles/project_ingest_40000_blocks.md, scaled from 40000 to 4096 blocks"),
     "ingest_tokens": (None, "no capture of the token path yet"),
+    "prefill_rows": (None, "no capture of the per-row scorer yet"),
 }
 
 
@@ -510,6 +511,67 @@ class PrefillWorkload(_Base):
         return self.Q.numel() * 2 + self.K_new.numel() * 2, self.k * 4
 
 
+class PrefillRowsWorkload(PrefillWorkload):
+    """The prefill chunk with per-row selection (QSA-style): every query row scores the
+    8192 blocks on its own and takes the 128 it has seen whole with the largest scores.
+    The chunk is the context's last 512 tokens (first_pos = 131072 - 512), so every row has
+    seen between 8160 and 8191 blocks whole."""
+
+    name = "prefill_rows"
+    topk = 128
+
+    def __init__(self, device, seed: int):
+        super().__init__(device, seed)
+        torch = self.torch
+        self.row_scores = torch.empty(2, self.R, self.n, dtype=torch.float32, device=device)
+        self.lists = torch.empty(2, self.R, self.topk, dtype=torch.int32, device=device)
+        self.first_pos = self.n * self.dims.block_size - self.R
+        torch.cuda.synchronize()
+
+    launches_per_step = 5  # ingest, project Q, fill, score rows, select rows
+
+    def step(self, Q=None, K_new=None):
+        hss, d, l = self.hss, self.dims, self.parity
+        hss.hss_project_kv_blocks(d, self.P, self.K_new if K_new is None else K_new, l,
+                                  self.new_ids, self.new_ids.numel(), self.A)
+        hss.hss_project_q(d, self.P, self.Q if Q is None else Q, self.R, self.Qp)
+        hss.hss_score_rows(d, self.Qp, self.R, self.A, l, self.table, self.n, self.row_scores[l])
+        hss.hss_select_rows(self.row_scores[l], self.R, self.n, self.first_pos, d.block_size,
+                            self.topk, self.lists[l])
+        self.parity ^= 1
+
+    dominant_kernel = "score_tc (per-row)"
+
+    def dominant(self):
+        for l in range(2):
+            self.hss.hss_score_rows(self.dims, self.Qp, self.R, self.A, l, self.table, self.n,
+                                    self.row_scores[l])
+
+    def describe(self):
+        d = self.dims
+        return (f"prefill chunk, per-row selection: {self.R} query rows x {d.num_q_heads} q "
+                f"heads (g {d.num_q_heads // d.num_kv_heads}) against {self.n} blocks, hd "
+                f"{d.head_dim}, r {d.r}; per step: project the chunk's "
+                f"{self.new_ids.numel()} blocks, project Q, per-row scores (tcgen05), per-row "
+                f"top-{self.topk} of the blocks each row has seen whole")
+
+    def e2e_step(self):
+        self.d_Q.copy_(self.h_Q, non_blocking=True)
+        self.d_K.copy_(self.h_K, non_blocking=True)
+        l = self.parity
+        self.step(Q=self.d_Q, K_new=self.d_K)
+        self.h_lists.copy_(self.lists[l], non_blocking=True)
+        self.torch.cuda.current_stream().synchronize()
+
+    def e2e_setup(self):
+        super().e2e_setup()
+        self.h_lists = self.torch.empty(self.R, self.topk, dtype=self.torch.int32).pin_memory()
+
+    @property
+    def e2e_bytes(self):
+        return self.Q.numel() * 2 + self.K_new.numel() * 2, self.R * self.topk * 4
+
+
 class IngestWorkload(_Base):
     """4096 new blocks projected into each of 32 layers, then one layer's 65536 blocks
     scored and ranked; skewed keys.  One step = 32 ingest calls + project Q + score + rank."""
@@ -674,7 +736,8 @@ class IngestTokensWorkload(IngestWorkload):
 
 
 WORKLOADS = {"decode": DecodeWorkload, "batched": BatchedWorkload, "prefill": PrefillWorkload,
-             "ingest": IngestWorkload, "ingest_tokens": IngestTokensWorkload}
+             "ingest": IngestWorkload, "ingest_tokens": IngestTokensWorkload,
+             "prefill_rows": PrefillRowsWorkload}
 
 
 # ----------------------------------------------------------------------------- oracle timing
@@ -687,7 +750,7 @@ def _bits(t):
 
 
 SAMPLE_BLOCKS = {"decode": 2048, "batched": 544, "prefill": 8, "ingest": 256,
-                 "ingest_tokens": 256}
+                 "ingest_tokens": 256, "prefill_rows": 8}
 
 
 class OracleSample:
@@ -706,8 +769,11 @@ class OracleSample:
 
         self.np, self.oracle, self.threads = np, oracle, threads
         self.tokens = name == "ingest_tokens"  # ingest through the oracle's cache write
+        self.rows = name == "prefill_rows"    # per-row scores and per-row selection
         if self.tokens:
             name = "ingest"
+        if self.rows:
+            name = "prefill"
         one = lambda d, mb=None: W.Dims(1, d.num_q_heads, d.num_kv_heads, d.head_dim, d.r,
                                         d.block_size, mb or d.max_blocks)
         # (dims, query rows, key distribution, blocks drawn, ingest per call, ingest per scored)
@@ -754,6 +820,13 @@ class OracleSample:
                 oracle.project_kv_blocks(self.P, self.K[pos], 0, bid, self.A,
                                          nthreads=self.threads)
         Qp = oracle.project_q(self.Q, self.P, nthreads=self.threads)
+        if self.rows:
+            d = c.dims
+            s, _, _ = oracle.score_rows(Qp.reshape(-1, d.num_q_heads, d.r), self.A, 0, ids,
+                                        nthreads=self.threads)
+            oracle.select_rows(s.astype(np.float32), m, m * d.block_size, d.block_size,
+                               min(128, max(1, m)))
+            return m
         offs = np.array([0, m], dtype=np.int64)
         s, _, _ = oracle.score_blocks(Qp, self.A, 0, ids, offs, nthreads=self.threads)
         oracle.rank_victims(s.astype(np.float32), offs, max(1, min(c.k_victims, m)))

@@ -227,6 +227,42 @@ hss_status hss_rank_victims(const float* scores, const int32_t* seq_offsets, int
                             int64_t total_blocks, int32_t k, int32_t* victims, void* stream);
 
 /*
+ * Per-row block scores (QSA-style selection, the host top-k of the page
+ * "metrale_model_layers/layers/qsa_select.rs" done on the GPU, with this predictor's score):
+ * for one sequence's chunk of query rows, each row on its own,
+ *   scores[row * num_blocks + j] = max over query heads h and the tokens t of block
+ *       block_table[j] of  sum_k Qp[row][h][k] * A_g[layer][block_table[j]][h / g][t][k]
+ * i.e. the block score of hss_score_blocks without the max over rows.  Runs on the tcgen05
+ * scorer (the dense prefill contraction).
+ *   Qp           device, [rows, num_q_heads, r] bf16, 16-byte aligned
+ *   block_table  device, [num_blocks] int32: the sequence's physical block ids, in order
+ *   scores       device, [rows, num_blocks] f32 (output)
+ * Supported: g = num_q_heads / num_kv_heads in {1, 2, 4, 8, 16}, block_size 16 or 32, and
+ * the tcgen05 scorer's shapes; otherwise HSS_ERR_UNSUPPORTED_SHAPE.  An id outside
+ * [0, max_blocks) scores -inf in every row (never selected) and raises HSS_ERR_OUT_OF_RANGE
+ * in *dev_status (if not NULL) and the library's device error word.
+ */
+hss_status hss_score_rows(const hss_dims* dims, const uint16_t* Qp, int32_t rows,
+                          const uint16_t* A_g, int32_t layer, const int32_t* block_table,
+                          int64_t num_blocks, float* scores, int32_t* dev_status, void* stream);
+
+/*
+ * Per-row top-k selection (the host top-k per row of the page
+ * "metrale_model_layers/layers/qsa_select.rs", QsaIndexer::prefill_select, on the GPU).
+ * Row r of a prefill chunk whose first row sits at position first_pos has seen the blocks
+ *   j < complete_r = min(num_blocks, (first_pos + r + 1) / block_size)
+ * whole; its list holds the topk of them with the largest scores[r * num_blocks + j],
+ * larger first, the lower index first among equal scores (-0 equals +0; NaN ranks like
+ * -inf, below every number), as indices j; lists[r * topk + i] = -1 where i >= complete_r.
+ *   scores  device, [rows, num_blocks] f32 (e.g. from hss_score_rows)
+ *   lists   device, [rows, topk] int32 (output); 1 <= topk <= HSS_MAX_VICTIMS
+ * The result is exact (integer output).
+ */
+hss_status hss_select_rows(const float* scores, int32_t rows, int64_t num_blocks,
+                           int64_t first_pos, int32_t block_size, int32_t topk, int32_t* lists,
+                           void* stream);
+
+/*
  * One predictor layer call in as few launches as the shape allows: project the newly
  * written blocks into A_g and the query rows into Qp (one launch), score every table
  * entry, and rank the victims of every sequence.  Results are the same as

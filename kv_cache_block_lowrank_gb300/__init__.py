@@ -41,7 +41,8 @@ EXPORTED = (
     "hss_project_kv_blocks", "hss_score_blocks", "hss_rank_victims", "hss_read_device_error",
     "hss_layer_step", "hss_layer_step_workspace_bytes", "hss_layer_step_static",
     "hss_score_blocks_masked",
-    "hss_layer_step_static_max_seqs", "hss_write_kv_tokens", "hss_self_test_wait_timeout",
+    "hss_layer_step_static_max_seqs", "hss_write_kv_tokens", "hss_score_rows",
+    "hss_select_rows", "hss_self_test_wait_timeout",
 )
 
 
@@ -102,6 +103,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.hss_project_kv_blocks.argtypes = [dp, vp, vp, i32, vp, i64, vp, vp, vp]
     lib.hss_write_kv_tokens.restype = i32
     lib.hss_write_kv_tokens.argtypes = [dp, vp, vp, vp, i64, vp, vp, i32, vp, vp]
+    lib.hss_score_rows.restype = i32
+    lib.hss_score_rows.argtypes = [dp, vp, i32, vp, i32, vp, i64, vp, vp, vp]
+    lib.hss_select_rows.restype = i32
+    lib.hss_select_rows.argtypes = [vp, i32, i64, i64, i32, i32, vp, vp]
     lib.hss_score_blocks.restype = i32
     lib.hss_score_blocks.argtypes = [dp, vp, i32, vp, i32, vp, vp, i32, i64, vp, i32, vp, vp]
     lib.hss_score_blocks_masked.restype = i32
@@ -194,6 +199,23 @@ def hss_write_kv_tokens(dims, P, K_tok, slots, num_tokens: int, K_cache, A_g, la
                                     _ptr(slots), int(num_tokens), _ptr(K_cache), _ptr(A_g),
                                     int(layer), _ptr(dev_status), _stream(stream))
     _check(st, "hss_write_kv_tokens")
+
+
+def hss_score_rows(dims, Qp, rows: int, A_g, layer: int, block_table, num_blocks: int, scores,
+                   dev_status=None, stream=None) -> None:
+    """scores[row, j] = max over heads and tokens of block_table[j] of Qp[row] . A_g."""
+    st = load().hss_score_rows(ctypes.byref(hss_dims.of(dims)), _ptr(Qp), int(rows), _ptr(A_g),
+                               int(layer), _ptr(block_table), int(num_blocks), _ptr(scores),
+                               _ptr(dev_status), _stream(stream))
+    _check(st, "hss_score_rows")
+
+
+def hss_select_rows(scores, rows: int, num_blocks: int, first_pos: int, block_size: int,
+                    topk: int, lists, stream=None) -> None:
+    """lists[r] = the topk blocks row r has seen whole, largest score first."""
+    st = load().hss_select_rows(_ptr(scores), int(rows), int(num_blocks), int(first_pos),
+                                int(block_size), int(topk), _ptr(lists), _stream(stream))
+    _check(st, "hss_select_rows")
 
 
 def hss_score_blocks(dims, Qp, rows_per_seq: int, A_g, layer: int, block_table, seq_offsets,

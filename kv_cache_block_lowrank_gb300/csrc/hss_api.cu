@@ -363,6 +363,55 @@ hss_status hss_layer_step(const hss_dims* dims, const uint16_t* P, const uint16_
     return HSS_OK;
 }
 
+hss_status hss_score_rows(const hss_dims* dims, const uint16_t* Qp, int32_t rows,
+                          const uint16_t* A_g, int32_t layer, const int32_t* block_table,
+                          int64_t num_blocks, float* scores, int32_t* dev_status, void* stream) {
+    hss_status st = check_dims(dims);
+    if (st != HSS_OK) return st;
+    if (layer < 0 || layer >= dims->num_layers) return HSS_ERR_OUT_OF_RANGE;
+    if (rows < 1 || num_blocks < 0 || num_blocks > 0x7FFFFFFF ||
+        static_cast<int64_t>(rows) * num_blocks > (int64_t{1} << 40))
+        return HSS_ERR_INVALID_ARGUMENT;
+    if (num_blocks == 0) return HSS_OK;
+    if (Qp == nullptr || A_g == nullptr || block_table == nullptr || scores == nullptr)
+        return HSS_ERR_NULL_POINTER;
+    if (!aligned16(Qp) || !aligned16(A_g) || (reinterpret_cast<uintptr_t>(scores) & 3u))
+        return HSS_ERR_MISALIGNED;
+    const int g = dims->num_q_heads / dims->num_kv_heads;
+    ScoreArgs a{};
+    a.Qp = Qp;
+    a.rows_per_seq = rows;
+    a.A_g = A_g;
+    a.layer_offset_slots = static_cast<int64_t>(layer) * dims->max_blocks;
+    a.max_blocks = dims->max_blocks;
+    a.table = block_table;
+    a.seq_offsets = nullptr;
+    a.num_seqs = 1;
+    a.total = num_blocks;
+    a.scores = scores;
+    a.num_q_heads = dims->num_q_heads;
+    a.num_kv_heads = dims->num_kv_heads;
+    a.r = dims->r;
+    a.block_size = dims->block_size;
+    a.dev_status = dev_status;
+    if ((g & (g - 1)) != 0 || g > 16 || !score_tc_supported(a)) return HSS_ERR_UNSUPPORTED_SHAPE;
+    return launch_score_tc_rows(a, static_cast<cudaStream_t>(stream));
+}
+
+hss_status hss_select_rows(const float* scores, int32_t rows, int64_t num_blocks,
+                           int64_t first_pos, int32_t block_size, int32_t topk, int32_t* lists,
+                           void* stream) {
+    if (rows < 0 || num_blocks < 0 || num_blocks > 0x7FFFFFFF || first_pos < 0 ||
+        block_size < 1 || topk < 1 || topk > HSS_MAX_VICTIMS)
+        return HSS_ERR_INVALID_ARGUMENT;
+    if (rows == 0) return HSS_OK;
+    if (lists == nullptr || (num_blocks > 0 && scores == nullptr)) return HSS_ERR_NULL_POINTER;
+    if ((reinterpret_cast<uintptr_t>(scores) & 3u) || (reinterpret_cast<uintptr_t>(lists) & 3u))
+        return HSS_ERR_MISALIGNED;
+    return launch_select_rows(scores, rows, num_blocks, first_pos, block_size, topk, lists,
+                              static_cast<cudaStream_t>(stream));
+}
+
 hss_status hss_read_device_error(int32_t* status, void* stream) {
     if (status == nullptr) return HSS_ERR_NULL_POINTER;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);

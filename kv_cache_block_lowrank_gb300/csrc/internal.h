@@ -126,9 +126,17 @@ hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream,
 bool score_decode_supported(const ScoreArgs& a);
 bool score_decode_inline_supported(const ScoreArgs& a, int32_t head_dim);
 hss_status launch_score_tc(const ScoreArgs& a, cudaStream_t stream);
+// Per-row scores of one sequence (a.num_seqs == 1, g = num_q_heads / num_kv_heads in
+// {1, 2, 4, 8, 16}, no masks): a.scores is [rows_per_seq, total]; a.seq_offsets may be null.
+hss_status launch_score_tc_rows(const ScoreArgs& a, cudaStream_t stream);
 bool score_tc_supported(const ScoreArgs& a);
 
 // ------------------------------------------------------------------- victims
+// Per-row selection: row r of scores [rows, n] takes its topk largest among the first
+// min(n, (first_pos + r + 1) / block_size) entries (lower index first on ties).
+hss_status launch_select_rows(const float* scores, int32_t rows, int64_t n, int64_t first_pos,
+                              int32_t block_size, int32_t topk, int32_t* lists,
+                              cudaStream_t stream);
 hss_status launch_rank_victims(const float* scores, const int32_t* seq_offsets, int32_t num_seqs,
                                int64_t total, int32_t k, int32_t* victims, cudaStream_t stream);
 

@@ -34,6 +34,19 @@ __device__ __forceinline__ uint32_t score_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Keys of the order the selection works in: ascending scores (victims), or descending
+// scores (DESC: the most relevant blocks first; NaN ranks like -inf, below every number).
+// Either way the words (key << 32 | index) are then taken smallest first.
+template <bool DESC>
+__device__ __forceinline__ uint32_t rank_key(float f) {
+    if constexpr (DESC) {
+        if (f != f) f = -INFINITY;
+        return ~score_key(f);
+    } else {
+        return score_key(f);
+    }
+}
+
 struct RankShared {
     uint32_t hist[2][256];
     uint32_t red_min[32];
@@ -111,7 +124,7 @@ __device__ void bitonic_sort(uint64_t* sel, int P) {
 
 // The sequence's keys, seen in one of two ways.  Key i lives at (slot i / THREADS, thread
 // i % THREADS), so a slot is a run of THREADS consecutive indices.
-template <int THREADS, bool IN_REGS>
+template <int THREADS, bool IN_REGS, bool DESC>
 struct KeySet {
     const float* sc;
     int n;
@@ -125,7 +138,7 @@ struct KeySet {
 #pragma unroll
             for (int j = 0; j < kKpt; ++j) {
                 const int i = j * THREADS + static_cast<int>(threadIdx.x);
-                r[j] = i < n ? score_key(__ldcg(&sc[i])) : 0u;
+                r[j] = i < n ? rank_key<DESC>(__ldcg(&sc[i])) : 0u;
             }
         }
     }
@@ -145,7 +158,7 @@ struct KeySet {
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {  // eight independent loads in flight
                     const int i = base + u * THREADS + static_cast<int>(threadIdx.x);
-                    b[u] = i < n ? score_key(__ldcg(&sc[i])) : 0u;
+                    b[u] = i < n ? rank_key<DESC>(__ldcg(&sc[i])) : 0u;
                 }
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
@@ -168,12 +181,12 @@ struct KeySet {
                 if (q == j) v = r[q];
             return v;
         } else {
-            return score_key(__ldcg(&sc[i]));
+            return rank_key<DESC>(__ldcg(&sc[i]));
         }
     }
 };
 
-template <int THREADS, bool IN_REGS>
+template <int THREADS, bool IN_REGS, bool DESC>
 __device__ void rank_with(const float* __restrict__ sc, int n, int k, int32_t* __restrict__ out,
                           uint64_t* sel, int sel_cap, RankShared* sh) {
     constexpr int kWarps = THREADS / 32;
@@ -182,7 +195,7 @@ __device__ void rank_with(const float* __restrict__ sc, int n, int k, int32_t* _
     const uint32_t lane_lt = (1u << lane) - 1u;
     const int take = n < k ? n : k;
 
-    KeySet<THREADS, IN_REGS> ks;
+    KeySet<THREADS, IN_REGS, DESC> ks;
     ks.load(sc, n);  // the loads are in flight while the histograms are cleared
     if (tid < 256) {
         sh->hist[0][tid] = 0;
@@ -208,7 +221,7 @@ __device__ void rank_with(const float* __restrict__ sc, int n, int k, int32_t* _
         const int rounds = (n + THREADS - 1) / THREADS;
         if constexpr (IN_REGS) {
 #pragma unroll
-            for (int j = 0; j < KeySet<THREADS, IN_REGS>::kKpt; ++j) {
+            for (int j = 0; j < KeySet<THREADS, IN_REGS, DESC>::kKpt; ++j) {
                 if (j < rounds) {
                     const int i = j * THREADS + tid;
                     fn(i < n, i < n ? ks.r[j] : 0u, i);
@@ -228,7 +241,7 @@ __device__ void rank_with(const float* __restrict__ sc, int n, int k, int32_t* _
     // words are sorted afterwards.
     auto collect = [&](auto&& pred) {
         if constexpr (IN_REGS) {
-            constexpr int kK = KeySet<THREADS, IN_REGS>::kKpt;
+            constexpr int kK = KeySet<THREADS, IN_REGS, DESC>::kKpt;
             const int rounds = (n + THREADS - 1) / THREADS;
             // The ballots are taken twice (count, then place) rather than kept in registers.
             uint32_t wcount = 0;
@@ -418,14 +431,14 @@ __device__ void rank_with(const float* __restrict__ sc, int n, int k, int32_t* _
 // calls it (THREADS = blockDim.x); sel [sel_cap] and sh are shared memory.  Scores are read
 // through L2 (ld.global.cg), so the function may also run in the kernel that wrote them,
 // after a fence.
-template <int THREADS>
+template <int THREADS, bool DESC = false>
 __device__ void rank_sequence(const float* __restrict__ sc, int n, int k,
                               int32_t* __restrict__ out, uint64_t* sel, int sel_cap,
                               RankShared* sh) {
     if (n <= THREADS * keys_per_thread<THREADS>())
-        rank_with<THREADS, true>(sc, n, k, out, sel, sel_cap, sh);
+        rank_with<THREADS, true, DESC>(sc, n, k, out, sel, sel_cap, sh);
     else
-        rank_with<THREADS, false>(sc, n, k, out, sel, sel_cap, sh);
+        rank_with<THREADS, false, DESC>(sc, n, k, out, sel, sel_cap, sh);
 }
 
 // Shared-memory bytes rank_sequence needs.

@@ -146,14 +146,88 @@ __global__ void fill_neg_inf(float* __restrict__ x, int64_t n) {
         x[i] = -INFINITY;
 }
 
+// Per-row scores (ROWG = g > 0): a thread takes one token's dot products with 32 query
+// vectors (32 / g query rows) at a time.  After the max over each row's g heads, a reduce-scatter over
+// the block's lanes leaves every lane with whole-block maxima of distinct rows:
+// at each step the lanes whose mask bit is set keep the upper half of their list and take
+// the partner's upper half, the others the lower half; once one value is left the remaining
+// steps are plain max reductions.
+template <int N, int CNT, int M>
+__device__ __forceinline__ void reduce_scatter(float (&x)[N], int lane) {
+    if constexpr (M > 0) {
+        if constexpr (CNT > 1) {
+            constexpr int H = CNT / 2;
+            const bool upper = (lane & M) != 0;
+#pragma unroll
+            for (int i = 0; i < H; ++i) {
+                const float send = upper ? x[i] : x[i + H];
+                const float keep = upper ? x[i + H] : x[i];
+                x[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, M));
+            }
+            reduce_scatter<N, H, M / 2>(x, lane);
+        } else {
+            x[0] = fmaxf(x[0], __shfl_xor_sync(0xffffffffu, x[0], M));
+            reduce_scatter<N, 1, M / 2>(x, lane);
+        }
+    }
+}
+
+// Row maxima of the 32 columns v[OFF .. OFF + 31] (vectors v0 .. v0 + 31, the first `valid`
+// real)
+// for the tokens of one block (BS lanes), max-combined into scores[row * stride + e].
+template <int G, int BS, int OFF>
+__device__ __forceinline__ void rows_to_scores(const uint32_t (&v)[128], int valid, int v0,
+                                               int lane, int rows, float* __restrict__ scores,
+                                               int64_t stride, int64_t e, bool e_ok) {
+    constexpr int V = 32 / G;
+    float x[V];
+    if (valid >= 32) {  // every column real: a plain 3-input max tree per row
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            float m = __uint_as_float(v[OFF + i * G]);
+#pragma unroll
+            for (int j = 1; j < G; j += 2)
+                m = j + 1 < G ? fmax3(m, __uint_as_float(v[OFF + i * G + j]),
+                                      __uint_as_float(v[OFF + i * G + j + 1]))
+                              : fmaxf(m, __uint_as_float(v[OFF + i * G + j]));
+            x[i] = m;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            float m = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+                if (i * G + j < valid) m = fmaxf(m, __uint_as_float(v[OFF + i * G + j]));
+            x[i] = m;
+        }
+    }
+    reduce_scatter<V, V, BS / 2>(x, lane);
+    constexpr int LOGV = V >= 32 ? 5 : V >= 16 ? 4 : V >= 8 ? 3 : V >= 4 ? 2 : V >= 2 ? 1 : 0;
+    constexpr int LOGB = BS == 32 ? 5 : 4;
+    constexpr int S = LOGV < LOGB ? LOGV : LOGB;  // scatter steps
+    constexpr int LEFT = V >> S;                  // values per lane at the end
+    const int lb = lane & (BS - 1);
+    if (!e_ok || (lb & ((1 << (LOGB - S)) - 1)) != 0) return;  // one writer per value
+    const int sel = lb >> (LOGB - S);
+#pragma unroll
+    for (int i = 0; i < LEFT; ++i) {
+        const int row = v0 / G + sel * LEFT + i;
+        if (row < rows) atomic_max_f32(scores + row * stride + e, x[i]);
+    }
+}
+
 // MASKED: the call passed ctx_len or row_pos0.  A template parameter, so the unmasked kernel
 // carries none of the mask arithmetic.  The mask pointers are kernel arguments of their own:
 // two more fields in TcParams made the unmasked kernel 7% slower on GB300.
-template <bool MASKED>
+// ROWG > 0: per-row scores (one sequence; g = ROWG query heads per kv head): scores is
+// [rows, total] and receives the max over heads and tokens for every (row, block).
+template <bool MASKED, int ROWG>
 __global__ void __launch_bounds__(kThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_q, const TcParams p,
-                    const int32_t* __restrict__ ctx_len, const int32_t* __restrict__ row_pos0) {
+                    const int32_t* __restrict__ ctx_len, const int32_t* __restrict__ row_pos0,
+                    const int64_t one_total) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -186,12 +260,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t acc = 0;
         for (int s = 0; s < p.num_seqs; ++s) {
             units_before[s] = acc;
-            offs[s] = p.seq_offsets[s];
-            const int64_t n = static_cast<int64_t>(p.seq_offsets[s + 1]) - p.seq_offsets[s];
+            // No offsets array: one sequence of `one_total` entries.
+            offs[s] = p.seq_offsets != nullptr ? p.seq_offsets[s] : 0;
+            const int64_t n = p.seq_offsets != nullptr
+                                  ? static_cast<int64_t>(p.seq_offsets[s + 1]) - p.seq_offsets[s]
+                                  : one_total;
             acc += static_cast<int64_t>(p.nkv) * ((n + p.bpt - 1) / p.bpt);
         }
         units_before[p.num_seqs] = acc;
-        offs[p.num_seqs] = p.seq_offsets[p.num_seqs];
+        offs[p.num_seqs] = p.seq_offsets != nullptr ? p.seq_offsets[p.num_seqs] : one_total;
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&a_full[s], 1);
             mbar_init(&a_empty[s], 1);
@@ -379,11 +456,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Query vectors of this warpgroup's columns: v0 .. v0 + 127, valid below nvec.
                 const int v0 = x.q * p.slice + nc * kNChunk + col0;
                 const int valid = min(128, p.nvec - v0);
-                if (valid > 0) {
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                       static_cast<uint32_t>(acc * kNChunk + col0);
+                if constexpr (ROWG > 0) {
+                    // All 128 columns to registers, the accumulator released, then 32 columns
+                    // (32 / g rows) at a time reduced and max-combined into the scores.
+                    uint32_t v[128];
+                    if (valid > 0) {
+                        tmem_ld_32x32b_x32(taddr, v);
+                        tmem_ld_32x32b_x32(taddr + 32, v + 32);
+                        tmem_ld_32x32b_x32(taddr + 64, v + 64);
+                        tmem_ld_32x32b_x32(taddr + 96, v + 96);
+                        tmem_ld_wait();
+                    }
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&t_empty[acc]);
+                    if (valid > 0) {
+                        const int blk = token / p.bs;
+                        const int64_t e = x.first + x.t * p.bpt + blk;
+                        bool e_ok = e < x.end;
+                        if (e_ok) {
+                            const int64_t id = p.table[e];
+                            e_ok = id >= 0 && id < p.max_blocks;
+                            if (!e_ok && x.c == 0 && x.q == 0 && nc == 0 &&
+                                (lane & (p.bs - 1)) == 0)
+                                raise_error(p.dev_status, p.lib_error, HSS_ERR_OUT_OF_RANGE);
+                        }
+                        const int64_t st = x.end - x.first, ee = e - x.first;
+                        if (p.bs == 16) {
+                            rows_to_scores<ROWG, 16, 0>(v, valid, v0, lane, p.rows, p.scores, st, ee, e_ok);
+                            if (valid > 32) rows_to_scores<ROWG, 16, 32>(v, valid - 32, v0 + 32, lane, p.rows, p.scores, st, ee, e_ok);
+                            if (valid > 64) rows_to_scores<ROWG, 16, 64>(v, valid - 64, v0 + 64, lane, p.rows, p.scores, st, ee, e_ok);
+                            if (valid > 96) rows_to_scores<ROWG, 16, 96>(v, valid - 96, v0 + 96, lane, p.rows, p.scores, st, ee, e_ok);
+                        } else {
+                            rows_to_scores<ROWG, 32, 0>(v, valid, v0, lane, p.rows, p.scores, st, ee, e_ok);
+                            if (valid > 32) rows_to_scores<ROWG, 32, 32>(v, valid - 32, v0 + 32, lane, p.rows, p.scores, st, ee, e_ok);
+                            if (valid > 64) rows_to_scores<ROWG, 32, 64>(v, valid - 64, v0 + 64, lane, p.rows, p.scores, st, ee, e_ok);
+                            if (valid > 96) rows_to_scores<ROWG, 32, 96>(v, valid - 96, v0 + 96, lane, p.rows, p.scores, st, ee, e_ok);
+                        }
+                    }
+                    continue;
+                } else if (valid > 0) {
                     any = true;
-                    const uint32_t taddr = tmem_base +
-                                           (static_cast<uint32_t>(quarter * 32) << 16) +
-                                           static_cast<uint32_t>(acc * kNChunk + col0);
                     uint32_t v[128];
                     tmem_ld_32x32b_x32(taddr, v);
                     tmem_ld_32x32b_x32(taddr + 32, v + 32);
@@ -422,6 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&t_empty[acc]);
             }
             if (!ok) break;
+            if constexpr (ROWG > 0) continue;  // per-row scores went out chunk by chunk
             if (!any) continue;  // none of this warpgroup's columns held a valid query vector
             // Max over the block's tokens: block_size consecutive lanes.
             for (int off = p.bs >> 1; off > 0; off >>= 1)
@@ -471,11 +587,33 @@ bool score_tc_supported(const ScoreArgs& a) {
     return L.stages >= 2;
 }
 
-hss_status launch_score_tc(const ScoreArgs& a, cudaStream_t stream) {
+namespace {
+
+using TcKernel = void (*)(CUtensorMap, CUtensorMap, TcParams, const int32_t*, const int32_t*,
+                          int64_t);
+
+TcKernel tc_kernel_for(bool masked, int rowg) {
+    switch (rowg) {
+        case 0: return masked ? score_tc_kernel<true, 0> : score_tc_kernel<false, 0>;
+        case 1: return score_tc_kernel<false, 1>;
+        case 2: return score_tc_kernel<false, 2>;
+        case 4: return score_tc_kernel<false, 4>;
+        case 8: return score_tc_kernel<false, 8>;
+        case 16: return score_tc_kernel<false, 16>;
+        default: return nullptr;
+    }
+}
+
+// rowg == 0: block scores (scores [total]); rowg == g: per-row scores of one sequence
+// (scores [rows_per_seq, total]).
+hss_status launch_tc(const ScoreArgs& a, int rowg, cudaStream_t stream) {
     if (a.total == 0) return HSS_OK;
     const DeviceInfo* dev = current_device_info();
     if (dev == nullptr) return HSS_ERR_CUDA;
     if (!score_tc_supported(a)) return HSS_ERR_UNSUPPORTED_SHAPE;
+    const bool masked = a.ctx_len != nullptr || a.row_pos0 != nullptr;
+    const TcKernel kern = tc_kernel_for(masked, rowg);
+    if (kern == nullptr || (rowg > 0 && (masked || a.num_seqs != 1))) return HSS_ERR_UNSUPPORTED_SHAPE;
     const TcLayout L = make_tc_layout(a.r, dev->max_smem_optin);
     if (L.stages < 2) return HSS_ERR_UNSUPPORTED_SHAPE;
     auto enc = tensor_map_encoder();
@@ -523,13 +661,14 @@ hss_status launch_score_tc(const ScoreArgs& a, cudaStream_t stream) {
         std::lock_guard<std::mutex> lk(g_smem_mu);
         const int d = dev->device & 63;
         if (g_smem_set[d] < L.total_bytes) {
-            if (cudaFuncSetAttribute(score_tc_kernel<false>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     L.total_bytes) != cudaSuccess ||
-                cudaFuncSetAttribute(score_tc_kernel<true>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     L.total_bytes) != cudaSuccess)
-                return HSS_ERR_CUDA;
+            const TcKernel all[] = {score_tc_kernel<false, 0>, score_tc_kernel<true, 0>,
+                                    score_tc_kernel<false, 1>, score_tc_kernel<false, 2>,
+                                    score_tc_kernel<false, 4>, score_tc_kernel<false, 8>,
+                                    score_tc_kernel<false, 16>};
+            for (TcKernel k : all)
+                if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         L.total_bytes) != cudaSuccess)
+                    return HSS_ERR_CUDA;
             g_smem_set[d] = L.total_bytes;
         }
     }
@@ -568,18 +707,27 @@ hss_status launch_score_tc(const ScoreArgs& a, cudaStream_t stream) {
     p.units_per_group = (units + groups - 1) / groups;
     const int grid = static_cast<int>(groups * p.nslices);
 
-    const int fill_grid = static_cast<int>(std::min<int64_t>((a.total + 255) / 256, 1024));
     float* scores = a.scores;
-    const int64_t total = a.total;
+    const int64_t total = rowg > 0 ? a.total * a.rows_per_seq : a.total;
+    const int fill_grid = static_cast<int>(std::min<int64_t>((total + 255) / 256, 1024));
     if (launch_pdl(fill_neg_inf, dim3(fill_grid), dim3(256), 0, stream, scores, total) !=
         cudaSuccess)
         return HSS_ERR_CUDA;
-    const bool masked = a.ctx_len != nullptr || a.row_pos0 != nullptr;
-    if (launch_pdl(masked ? score_tc_kernel<true> : score_tc_kernel<false>, dim3(grid),
-                   dim3(kThreads), L.total_bytes, stream, tmap_a, tmap_q, p, a.ctx_len,
-                   a.row_pos0) != cudaSuccess)
+    const int64_t one_total = a.total;
+    if (launch_pdl(kern, dim3(grid), dim3(kThreads), L.total_bytes, stream, tmap_a, tmap_q, p,
+                   a.ctx_len, a.row_pos0, one_total) != cudaSuccess)
         return HSS_ERR_CUDA;
     return HSS_OK;
+}
+
+}  // namespace
+
+hss_status launch_score_tc(const ScoreArgs& a, cudaStream_t stream) {
+    return launch_tc(a, 0, stream);
+}
+
+hss_status launch_score_tc_rows(const ScoreArgs& a, cudaStream_t stream) {
+    return launch_tc(a, a.num_q_heads / a.num_kv_heads, stream);
 }
 
 }  // namespace hss
