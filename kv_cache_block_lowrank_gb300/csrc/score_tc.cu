@@ -172,16 +172,16 @@ __device__ __forceinline__ void reduce_scatter(float (&x)[N], int lane) {
     }
 }
 
-// Row maxima of the 32 columns v[OFF .. OFF + 31] (vectors v0 .. v0 + 31, the first `valid`
-// real)
+// Row maxima of the COLS columns v[OFF .. OFF + COLS - 1] (vectors v0 .. v0 + COLS - 1, the
+// first `valid` real)
 // for the tokens of one block (BS lanes), max-combined into scores[row * stride + e].
-template <int G, int BS, int OFF>
+template <int G, int BS, int OFF, int COLS>
 __device__ __forceinline__ void rows_to_scores(const uint32_t (&v)[128], int valid, int v0,
                                                int lane, int rows, float* __restrict__ scores,
                                                int64_t stride, int64_t e, bool e_ok) {
-    constexpr int V = 32 / G;
+    constexpr int V = COLS / G;
     float x[V];
-    if (valid >= 32) {  // every column real: a plain 3-input max tree per row
+    if (valid >= COLS) {  // every column real: a plain 3-input max tree per row
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             float m = __uint_as_float(v[OFF + i * G]);
@@ -204,11 +204,62 @@ __device__ __forceinline__ void rows_to_scores(const uint32_t (&v)[128], int val
     }
     reduce_scatter<V, V, BS / 2>(x, lane);
     constexpr int LOGV = V >= 32 ? 5 : V >= 16 ? 4 : V >= 8 ? 3 : V >= 4 ? 2 : V >= 2 ? 1 : 0;
+    static_assert(V <= 32, "at most 32 row values per lane");
     constexpr int LOGB = BS == 32 ? 5 : 4;
     constexpr int S = LOGV < LOGB ? LOGV : LOGB;  // scatter steps
     constexpr int LEFT = V >> S;                  // values per lane at the end
     const int lb = lane & (BS - 1);
     if (!e_ok || (lb & ((1 << (LOGB - S)) - 1)) != 0) return;  // one writer per value
+    const int sel = lb >> (LOGB - S);
+#pragma unroll
+    for (int i = 0; i < LEFT; ++i) {
+        const int row = v0 / G + sel * LEFT + i;
+        if (row < rows) atomic_max_f32(scores + row * stride + e, x[i]);
+    }
+}
+
+// Max over each row's G heads for 64 columns va[0 .. 63] (the first `valid` real) into
+// x[XOFF .. XOFF + 64 / G).
+template <int G, int XOFF, int V>
+__device__ __forceinline__ void group_max64(const uint32_t (&va)[64], int valid, float (&x)[V]) {
+    constexpr int R = 64 / G;
+    if (valid >= 64) {
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            float m = __uint_as_float(va[i * G]);
+#pragma unroll
+            for (int j = 1; j < G; j += 2)
+                m = j + 1 < G ? fmax3(m, __uint_as_float(va[i * G + j]),
+                                      __uint_as_float(va[i * G + j + 1]))
+                              : fmaxf(m, __uint_as_float(va[i * G + j]));
+            x[XOFF + i] = m;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            float m = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+                if (i * G + j < valid) m = fmaxf(m, __uint_as_float(va[i * G + j]));
+            x[XOFF + i] = m;
+        }
+    }
+}
+
+// Whole-block maxima of the V row values x (rows v0 / G ..): reduce-scatter over the block's
+// BS lanes, then one float atomic max per value into scores[row * stride + e].
+template <int G, int BS, int V>
+__device__ __forceinline__ void scatter_rows(float (&x)[V], int v0, int lane, int rows,
+                                             float* __restrict__ scores, int64_t stride,
+                                             int64_t e, bool e_ok) {
+    reduce_scatter<V, V, BS / 2>(x, lane);
+    constexpr int LOGV = V >= 32 ? 5 : V >= 16 ? 4 : V >= 8 ? 3 : V >= 4 ? 2 : V >= 2 ? 1 : 0;
+    static_assert(V <= 32, "at most 32 row values per lane");
+    constexpr int LOGB = BS == 32 ? 5 : 4;
+    constexpr int S = LOGV < LOGB ? LOGV : LOGB;
+    constexpr int LEFT = V >> S;
+    const int lb = lane & (BS - 1);
+    if (!e_ok || (lb & ((1 << (LOGB - S)) - 1)) != 0) return;
     const int sel = lb >> (LOGB - S);
 #pragma unroll
     for (int i = 0; i < LEFT; ++i) {
@@ -458,9 +509,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int valid = min(128, p.nvec - v0);
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        static_cast<uint32_t>(acc * kNChunk + col0);
-                if constexpr (ROWG > 0) {
-                    // All 128 columns to registers, the accumulator released, then 32 columns
-                    // (32 / g rows) at a time reduced and max-combined into the scores.
+                if constexpr (ROWG >= 4) {
+                    // 128 / g <= 32 rows: the columns come in two halves of 64, each folded to
+                    // row maxima at once; the accumulator is released before the shuffles.
+                    constexpr int V = 128 / ROWG;
+                    float xr[V];
+                    if (valid > 0) {
+                        uint32_t va[64];
+                        tmem_ld_32x32b_x32(taddr, va);
+                        tmem_ld_32x32b_x32(taddr + 32, va + 32);
+                        tmem_ld_wait();
+                        group_max64<ROWG, 0>(va, valid, xr);
+                        tmem_ld_32x32b_x32(taddr + 64, va);
+                        tmem_ld_32x32b_x32(taddr + 96, va + 32);
+                        tmem_ld_wait();
+                        group_max64<ROWG, V / 2>(va, valid - 64, xr);
+                    }
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&t_empty[acc]);
+                    if (valid > 0) {
+                        const int blk = token / p.bs;
+                        const int64_t e = x.first + x.t * p.bpt + blk;
+                        bool e_ok = e < x.end;
+                        if (e_ok) {
+                            const int64_t id = p.table[e];
+                            e_ok = id >= 0 && id < p.max_blocks;
+                            if (!e_ok && x.c == 0 && x.q == 0 && nc == 0 &&
+                                (lane & (p.bs - 1)) == 0)
+                                raise_error(p.dev_status, p.lib_error, HSS_ERR_OUT_OF_RANGE);
+                        }
+                        const int64_t st = x.end - x.first, ee = e - x.first;
+                        if (p.bs == 16)
+                            scatter_rows<ROWG, 16>(xr, v0, lane, p.rows, p.scores, st, ee, e_ok);
+                        else
+                            scatter_rows<ROWG, 32>(xr, v0, lane, p.rows, p.scores, st, ee, e_ok);
+                    }
+                    continue;
+                } else if constexpr (ROWG > 0) {
+                    // g 1 or 2: all 128 columns to registers, the accumulator released, then
+                    // 32 columns (32 / g rows) at a time.
                     uint32_t v[128];
                     if (valid > 0) {
                         tmem_ld_32x32b_x32(taddr, v);
@@ -485,15 +573,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         const int64_t st = x.end - x.first, ee = e - x.first;
                         if (p.bs == 16) {
-                            rows_to_scores<ROWG, 16, 0>(v, valid, v0, lane, p.rows, p.scores, st, ee, e_ok);
-                            if (valid > 32) rows_to_scores<ROWG, 16, 32>(v, valid - 32, v0 + 32, lane, p.rows, p.scores, st, ee, e_ok);
-                            if (valid > 64) rows_to_scores<ROWG, 16, 64>(v, valid - 64, v0 + 64, lane, p.rows, p.scores, st, ee, e_ok);
-                            if (valid > 96) rows_to_scores<ROWG, 16, 96>(v, valid - 96, v0 + 96, lane, p.rows, p.scores, st, ee, e_ok);
+                            rows_to_scores<ROWG, 16, 0, 32>(v, valid, v0, lane, p.rows, p.scores, st, ee, e_ok);
+                            if (valid > 32) rows_to_scores<ROWG, 16, 32, 32>(v, valid - 32, v0 + 32, lane, p.rows, p.scores, st, ee, e_ok);
+                            if (valid > 64) rows_to_scores<ROWG, 16, 64, 32>(v, valid - 64, v0 + 64, lane, p.rows, p.scores, st, ee, e_ok);
+                            if (valid > 96) rows_to_scores<ROWG, 16, 96, 32>(v, valid - 96, v0 + 96, lane, p.rows, p.scores, st, ee, e_ok);
                         } else {
-                            rows_to_scores<ROWG, 32, 0>(v, valid, v0, lane, p.rows, p.scores, st, ee, e_ok);
-                            if (valid > 32) rows_to_scores<ROWG, 32, 32>(v, valid - 32, v0 + 32, lane, p.rows, p.scores, st, ee, e_ok);
-                            if (valid > 64) rows_to_scores<ROWG, 32, 64>(v, valid - 64, v0 + 64, lane, p.rows, p.scores, st, ee, e_ok);
-                            if (valid > 96) rows_to_scores<ROWG, 32, 96>(v, valid - 96, v0 + 96, lane, p.rows, p.scores, st, ee, e_ok);
+                            rows_to_scores<ROWG, 32, 0, 32>(v, valid, v0, lane, p.rows, p.scores, st, ee, e_ok);
+                            if (valid > 32) rows_to_scores<ROWG, 32, 32, 32>(v, valid - 32, v0 + 32, lane, p.rows, p.scores, st, ee, e_ok);
+                            if (valid > 64) rows_to_scores<ROWG, 32, 64, 32>(v, valid - 64, v0 + 64, lane, p.rows, p.scores, st, ee, e_ok);
+                            if (valid > 96) rows_to_scores<ROWG, 32, 96, 32>(v, valid - 96, v0 + 96, lane, p.rows, p.scores, st, ee, e_ok);
                         }
                     }
                     continue;
