@@ -11,6 +11,10 @@
 //   warp 1      TMEM allocator and MMA issuer: tcgen05.mma M=128, N=r, K=16 steps, fp32
 //               accumulators double-buffered in TMEM (2 x r columns)
 //   warps 2..5  epilogue: tcgen05.ld a row per thread, round to bf16, store the row
+//   warps 6..9  cache copy (token/slot mode with a cache only): each tile's key rows, already
+//               in shared memory, go to their slots in the paged key cache; the stage is free
+//               once the MMAs and all four copy warps are done with it (no barrier among the
+//               copy warps: each arrives on its own, so a wait that runs out cannot strand one)
 // P^T stays resident in shared memory (K-major, 128B swizzle) for the whole kernel.
 // The work is HBM-bound (head_dim * 2 bytes in, r * 2 bytes out per row); the tensor
 // cores only keep the arithmetic far below the memory time.
@@ -27,7 +31,7 @@ namespace {
 constexpr int kBM = 128;            // rows per tile = UMMA M
 constexpr int kChunkElems = 64;     // bf16 elements per 128-byte swizzled row segment
 constexpr int kChunkBytes = kBM * 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer, MMA, 4 epilogue warps, 4 cache-copy warps
 constexpr int kMaxStages = 6;
 
 struct ProjLayout {
@@ -111,9 +115,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t num_tiles = p.seg[0].tiles + p.seg[1].tiles;
 
     if (threadIdx.x == 0) {
+        const bool copy = p.seg[0].cache != nullptr || p.seg[1].cache != nullptr;
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], copy ? 5 : 1);  // the MMAs' commit (+ each copy warp)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
@@ -241,6 +246,63 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+    } else if (warp >= 6) {
+        // Cache copy: warp 6 + w takes rows 32w .. 32w + 31 of each tile, read from the
+        // swizzled stage and written to K_cache[slot][h].
+        const bool copy = p.seg[0].cache != nullptr || p.seg[1].cache != nullptr;
+        if (copy) {
+            const int cw = warp - 6;
+            const int row_bytes = p.head_dim * 2;
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+                const bool ok = mbar_wait(&full[stage], phase);
+                if (__any_sync(0xffffffffu, !ok) || *(volatile int*)abort_flag) {
+                    if (lane == 0) {
+                        raise_error(p.dev_status, p.lib_error, HSS_ERR_DEVICE_TIMEOUT);
+                        *(volatile int*)abort_flag = 1;
+                    }
+                    break;
+                }
+                const bool second = tile >= p.seg[0].tiles;
+                const ProjSegment& sg = second ? p.seg[1] : p.seg[0];
+                const int64_t local = second ? tile - p.seg[0].tiles : tile;
+                if (sg.cache != nullptr) {
+                    // This warp's 32 rows: every lane looks up one row's destination at once,
+                    // then the rows go out two at a time (16 lanes x 16 bytes per row piece).
+                    const uint8_t* src = sA + stage * stage_bytes;
+                    const int my_rr = cw * 32 + lane;
+                    const int64_t my_m = local * kBM + my_rr;
+                    int64_t my_dst = -1;  // element offset of the row in the cache, or -1
+                    if (my_m < sg.num_rows) {
+                        const int64_t i = my_m / p.num_kv_heads;
+                        const int64_t h = my_m - i * p.num_kv_heads;
+                        const int64_t sl = sg.slots[i];
+                        if (sl >= 0 && sl < p.max_blocks * p.block_size)
+                            my_dst = (sl * p.num_kv_heads + h) * p.head_dim;
+                    }
+                    for (int k = 0; k < 16; ++k) {
+                        const int pick = 2 * k + (lane >> 4);
+                        const int64_t dst = __shfl_sync(0xffffffffu, my_dst, pick);
+                        const int rr = cw * 32 + pick;
+                        if (dst < 0) continue;
+                        uint8_t* drow = reinterpret_cast<uint8_t*>(sg.cache + dst);
+                        for (int cb = (lane & 15) * 16; cb < row_bytes; cb += 256) {
+                            const int kc = cb >> 7, c16 = (cb & 127) >> 4;
+                            const uint4 val = *reinterpret_cast<const uint4*>(
+                                src + kc * kChunkBytes + rr * 128 + ((c16 ^ (rr & 7)) << 4));
+                            *reinterpret_cast<uint4*>(drow + cb) = val;
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[stage]);  // this warp is done with the stage
+                if (++stage == stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
     } else {
         // Epilogue: warp w reads TMEM lanes 32 * (w % 4) .. + 31, one output row per thread.
         const int quarter = warp & 3;
@@ -274,19 +336,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int t = static_cast<int>(sl - blk * p.block_size);
                         dst = sg.out + (((p.layer_slots + blk) * p.num_kv_heads + h) *
                                             p.block_size + t) * static_cast<int64_t>(r);
-                        if (sg.cache != nullptr) {  // the key row, still in L2, to the cache
-                            const uint4* src =
-                                reinterpret_cast<const uint4*>(sg.X + m * p.head_dim);
-                            uint4* cd = reinterpret_cast<uint4*>(
-                                sg.cache + (sl * p.num_kv_heads + h) * p.head_dim);
-                            for (int c = 0; c < p.head_dim / 8; c += 8) {
-                                uint4 b[8];
-#pragma unroll
-                                for (int u = 0; u < 8; ++u) b[u] = __ldg(src + c + u);
-#pragma unroll
-                                for (int u = 0; u < 8; ++u) cd[c + u] = b[u];
-                            }
-                        }
                     } else if (sl >= 0 && h == 0) {
                         raise_error(p.dev_status, p.lib_error, HSS_ERR_OUT_OF_RANGE);
                     }
