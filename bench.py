@@ -49,6 +49,8 @@ def parse_args(argv=None):
                    help="launch every call from the host instead of replaying a CUDA graph")
     p.add_argument("--unfused", action="store_true",
                    help="decode: four separate calls per layer instead of hss_layer_step")
+    p.add_argument("--layers", type=int, default=32,
+                   help="ingest workloads: layers written per step (1: a small case for ncu)")
     return p.parse_args(argv)
 
 
@@ -192,8 +194,8 @@ TRAFFIC = {
     # captured on a 40000-block launch; traffic grows with the blocks, so scaled to 4096
     "ingest": (round((1310970000 + 305094400) * 4096 / 40000),
                "profiles/project_ingest_40000_blocks.md, scaled from 40000 to 4096 blocks"),
-    "ingest_tokens": (None, "no capture of the token path yet"),
-    "prefill_rows": (None, "no capture of the per-row scorer yet"),
+    "ingest_tokens": (None, "profiles/project_tokens_65536.md: pending capture"),
+    "prefill_rows": (157009664 + 3350272, "profiles/score_tc_prefill_rows.md"),
 }
 
 
@@ -578,12 +580,13 @@ class IngestWorkload(_Base):
 
     name = "ingest"
 
-    def __init__(self, device, seed: int):
+    def __init__(self, device, seed: int, layers: int = 32):
         super().__init__(device)
         import workloads as W
 
         torch, hss = self.torch, self.hss
-        self.case = c = W.ingest(seed=seed, device=device)
+        self.case = c = W.ingest(seed=seed, device=device, layers=layers,
+                                 score_layer=min(17, layers - 1))
         self.dims = d = c.dims
         self.L = d.num_layers
         self.n = c.total_blocks
@@ -673,8 +676,8 @@ class IngestTokensWorkload(IngestWorkload):
 
     name = "ingest_tokens"
 
-    def __init__(self, device, seed: int):
-        super().__init__(device, seed)
+    def __init__(self, device, seed: int, layers: int = 32):
+        super().__init__(device, seed, layers)
         torch, d = self.torch, self.dims
         bs, nkv, hd = d.block_size, d.num_kv_heads, d.head_dim
         ids = self.new_ids.to(torch.int64)
@@ -914,6 +917,8 @@ def run_hss(args):
 
     if args.workload == "decode":
         wl = DecodeWorkload(device, args.seed + rank, unfused=args.unfused)
+    elif args.workload in ("ingest", "ingest_tokens"):
+        wl = WORKLOADS[args.workload](device, args.seed + rank, layers=args.layers)
     else:
         wl = WORKLOADS[args.workload](device, args.seed + rank)
     peaks = measured_peaks()
