@@ -89,6 +89,38 @@ __device__ void bitonic_sort(uint64_t* sel, int P) {
         __syncthreads();
         return;
     }
+    if (P <= THREADS) {
+        // One element per thread.  Every thread runs the shuffle stages (threads past the end
+        // hold the largest word), so no branch surrounds them.
+        const bool act = tid < P;
+        uint64_t v = act ? sel[tid] : ~0ull;
+#pragma unroll
+        for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+            for (int stride = size >> 1; stride > 0; stride >>= 1) v = cx_shfl(v, tid, stride, size);
+        if (act) sel[tid] = v;
+        __syncthreads();
+        for (int size = 64; size <= P; size <<= 1) {
+            for (int stride = size >> 1; stride >= 32; stride >>= 1) {
+                if (tid < (P >> 1)) {
+                    const int i = 2 * tid - (tid & (stride - 1));
+                    const int j = i + stride;
+                    const uint64_t a = sel[i], b = sel[j];
+                    if ((a > b) == ((i & size) == 0)) {
+                        sel[i] = b;
+                        sel[j] = a;
+                    }
+                }
+                __syncthreads();
+            }
+            v = act ? sel[tid] : ~0ull;
+#pragma unroll
+            for (int stride = 16; stride > 0; stride >>= 1) v = cx_shfl(v, tid, stride, size);
+            if (act) sel[tid] = v;
+            __syncthreads();
+        }
+        return;
+    }
     // Sizes up to 32: each warp's 32 consecutive elements sort in registers at once.
     for (int i = tid; i < P; i += THREADS) {
         uint64_t v = sel[i];
@@ -242,15 +274,14 @@ __device__ void rank_with(const float* __restrict__ sc, int n, int k, int32_t* _
     auto collect = [&](auto&& pred) {
         if constexpr (IN_REGS) {
             constexpr int kK = KeySet<THREADS, IN_REGS, DESC>::kKpt;
-            const int rounds = (n + THREADS - 1) / THREADS;
             // The ballots are taken twice (count, then place) rather than kept in registers.
+            // No branch around them: `i < n` already drops the slots past the end, and a
+            // ballot under a condition costs a reconvergence point per slot.
             uint32_t wcount = 0;
 #pragma unroll
             for (int j = 0; j < kK; ++j) {
-                if (j < rounds) {  // uniform: every lane of every warp takes the same branches
-                    const int i = j * THREADS + tid;
-                    wcount += __popc(__ballot_sync(0xffffffffu, i < n && pred(ks.r[j])));
-                }
+                const int i = j * THREADS + tid;
+                wcount += __popc(__ballot_sync(0xffffffffu, i < n && pred(ks.r[j])));
             }
             if (lane == 0) sh->warp_tot[warp] = wcount;
             __syncthreads();
@@ -258,18 +289,13 @@ __device__ void rank_with(const float* __restrict__ sc, int n, int k, int32_t* _
             for (int w = 0; w < warp; ++w) base += sh->warp_tot[w];
 #pragma unroll
             for (int j = 0; j < kK; ++j) {
-                if (j < rounds) {
-                    const int i = j * THREADS + tid;
-                    const bool pick = i < n && pred(ks.r[j]);
-                    const uint32_t ball = __ballot_sync(0xffffffffu, pick);
-                    if (pick) {
-                        const uint32_t pos = base + __popc(ball & lane_lt);
-                        if (pos < static_cast<uint32_t>(sel_cap))
-                            sel[pos] = (static_cast<uint64_t>(ks.r[j]) << 32) |
-                                       static_cast<uint32_t>(i);
-                    }
-                    base += __popc(ball);
-                }
+                const int i = j * THREADS + tid;
+                const bool pick = i < n && pred(ks.r[j]);
+                const uint32_t ball = __ballot_sync(0xffffffffu, pick);
+                const uint32_t pos = base + __popc(ball & lane_lt);
+                if (pick && pos < static_cast<uint32_t>(sel_cap))
+                    sel[pos] = (static_cast<uint64_t>(ks.r[j]) << 32) | static_cast<uint32_t>(i);
+                base += __popc(ball);
             }
         } else {
             for_each_uniform([&](bool valid, uint32_t key, int i) {
