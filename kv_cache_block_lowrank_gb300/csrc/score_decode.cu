@@ -87,6 +87,12 @@ struct DecodeParams {
     int32_t nowait;
 };
 
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* addr, int v) {
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
                                                uint32_t a2, uint32_t a3, uint32_t b0,
                                                uint32_t b1) {
@@ -454,7 +460,9 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
     uint64_t* sel = reinterpret_cast<uint64_t*>(rank_smem);
     rankdev::RankShared* sh = reinterpret_cast<rankdev::RankShared*>(sel + p.sel_cap);
     int* todo = reinterpret_cast<int*>(sh + 1);  // [todo_cap + 1]
-    if (lane == 0) __threadfence();  // this warp's scores before the CTA's count
+    // The barrier orders every warp's scores before thread 0's count, which is a release at
+    // GPU scope (cumulative over what the barrier made visible to it); the count of the CTA
+    // that completes a sequence is also an acquire, so that CTA sees every other CTA's scores.
     __syncthreads();
     if (threadIdx.x == 0) {
         int ntodo = 0;
@@ -472,7 +480,7 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
                 if (a >= ce) break;
                 const int64_t cnt = min(ce, b) - max(cb, a);
                 if (cnt <= 0) continue;
-                const int old = atomicAdd(&p.counters[q], static_cast<int>(cnt));
+                const int old = atom_add_acq_rel_gpu(&p.counters[q], static_cast<int>(cnt));
                 if (old + cnt == b - a && ntodo < p.todo_cap) todo[1 + ntodo++] = q;
             }
         }
@@ -480,7 +488,6 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
     }
     __syncthreads();
     const int ntodo = todo[0];
-    if (ntodo > 0) __threadfence();  // every other CTA's scores of these sequences are visible
     for (int t = 0; t < ntodo; ++t) {
         const int q = todo[1 + t];
         const int64_t a = __ldg(&p.seq_offsets[q]);
