@@ -49,6 +49,8 @@ def parse_args(argv=None):
                    help="launch every call from the host instead of replaying a CUDA graph")
     p.add_argument("--unfused", action="store_true",
                    help="decode: four separate calls per layer instead of hss_layer_step")
+    p.add_argument("--cpu-threads", type=int, default=0,
+                   help="threads for the oracle's CPU legs (0: every core this process may use)")
     p.add_argument("--layers", type=int, default=32,
                    help="ingest workloads: layers written per step (1: a small case for ncu)")
     return p.parse_args(argv)
@@ -869,7 +871,7 @@ def run_reference(args):
     rank, world, local = dist_env()
     if rank != 0:
         return 0
-    threads = cpu_threads()
+    threads = args.cpu_threads or cpu_threads()
     orc = OracleSample(args.workload, args.seed, threads)
     m_full = SAMPLE_BLOCKS[args.workload]
     # Per-block cost, to size each step's sample so the whole run takes about a minute.
@@ -1012,7 +1014,7 @@ def run_hss(args):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        threads = cpu_threads()
+        threads = args.cpu_threads or cpu_threads()
         orc = OracleSample(args.workload, args.seed, threads)
         m = SAMPLE_BLOCKS[args.workload]
         scored, el, calls = orc.time(m, 10.0)
