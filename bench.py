@@ -190,7 +190,7 @@ def measured_peaks():
 # dram__bytes_write.sum) from the ncu captures summarised in profiles/, or None when the
 # kernel has changed since its capture.
 TRAFFIC = {
-    "decode": (16853504 + 0, "profiles/score_decode_plain.md"),
+    "decode": (16853248 + 0, "profiles/score_decode_plain.md"),
     "batched": (283584000 + 3072512, "profiles/score_decode_batched.md"),
     "prefill": (140040192 + 3555584, "profiles/score_tc_prefill.md"),
     # captured on a 40000-block launch; traffic grows with the blocks, so scaled to 4096
@@ -257,22 +257,23 @@ class DecodeWorkload(_Base):
         self.scores = torch.empty(self.L, self.n, dtype=torch.float32, device=device)
         self.victims = torch.empty(self.L, 1, self.k, dtype=torch.int32, device=device)
         self.ws_bytes = hss.hss_layer_step_workspace_bytes(1)
+        self.hdims = hss.hss_dims.of(d)
         self.ws = torch.zeros(self.ws_bytes // 4, dtype=torch.int32, device=device)
         torch.cuda.synchronize()
 
     units_per_step = property(lambda self: self.L * self.n)
     launches_per_step = property(lambda self: self.L * (4 if self.unfused else 2))
 
-    def layer_call(self, l: int, K_new=None, Q=None):
+    def layer_call(self, l: int, K_new=None, Q=None, stream=None):
         hss, d = self.hss, self.dims
         K_new = self.K_new[l] if K_new is None else K_new
         Q = self.Q[l] if Q is None else Q
         if not self.unfused:
             # Qp = NULL: the caller wants scores and victims, not the projected queries, so the
-            # decode scorer projects them itself.
-            hss.hss_layer_step(d, self.P, K_new, self.new_ids, 1, Q, 1, None, self.A, l,
+            # decode scorer projects them itself.  The dims go in as the prebuilt C struct.
+            hss.hss_layer_step(self.hdims, self.P, K_new, self.new_ids, 1, Q, 1, None, self.A, l,
                                self.table, self.offs, 1, self.n, self.scores[l], self.k,
-                               self.victims[l], self.ws, self.ws_bytes)
+                               self.victims[l], self.ws, self.ws_bytes, stream=stream)
             return
         hss.hss_project_kv_blocks(d, self.P, K_new, l, self.new_ids, 1, self.A)
         hss.hss_project_q(d, self.P, Q, 1, self.Qp[l])
@@ -329,8 +330,9 @@ class DecodeWorkload(_Base):
 
     def e2e_step(self):
         self.d_in.copy_(self.h_in, non_blocking=True)
+        stream = self.torch.cuda.current_stream().cuda_stream  # one lookup per step
         for l in range(self.L):
-            self.layer_call(l, K_new=self.d_K[l], Q=self.d_Q[l])
+            self.layer_call(l, K_new=self.d_K[l], Q=self.d_Q[l], stream=stream)
         self.h_vic.copy_(self.victims, non_blocking=True)
         self.torch.cuda.current_stream().synchronize()
 
