@@ -147,6 +147,11 @@ def _stream(stream) -> Optional[int]:
     if stream is None:
         import torch
 
+        # The raw handle of the current stream: the same value as
+        # torch.cuda.current_stream().cuda_stream without building a Stream object.
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            return raw(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
         return stream

@@ -435,6 +435,46 @@ static bool encode_rows_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace {
+
+// A tensor map only encodes an address and a shape, so one encoded for (X, rows, head_dim)
+// serves every later call with the same three: a few recent maps are kept (a decode step
+// projects the same small buffers layer after layer).
+struct MapCacheEntry {
+    const uint16_t* X = nullptr;
+    int64_t rows = 0;
+    int32_t head_dim = 0;
+    CUtensorMap map;
+};
+constexpr int kMapCache = 8;
+MapCacheEntry g_map_cache[kMapCache];
+int g_map_next = 0;
+std::mutex g_map_mu;
+
+bool rows_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, const uint16_t* X,
+              int64_t rows, int32_t head_dim) {
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        for (const MapCacheEntry& e : g_map_cache) {
+            if (e.X == X && e.rows == rows && e.head_dim == head_dim) {
+                *map = e.map;
+                return true;
+            }
+        }
+    }
+    if (!encode_rows_map(enc, map, X, rows, head_dim)) return false;
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    MapCacheEntry& e = g_map_cache[g_map_next];
+    g_map_next = (g_map_next + 1) % kMapCache;
+    e.X = X;
+    e.rows = rows;
+    e.head_dim = head_dim;
+    e.map = *map;
+    return true;
+}
+
+}  // namespace
+
 hss_status launch_project2(const ProjectArgs& a0, const ProjectArgs* a1, cudaStream_t stream) {
     const int64_t rows0 = a0.num_rows, rows1 = a1 != nullptr ? a1->num_rows : 0;
     if (rows0 == 0 && rows1 == 0) return HSS_OK;
@@ -450,9 +490,9 @@ hss_status launch_project2(const ProjectArgs& a0, const ProjectArgs* a1, cudaStr
     const ProjectArgs* s0 = rows0 > 0 ? &a0 : a1;
     const ProjectArgs* s1 = rows0 > 0 && rows1 > 0 ? a1 : nullptr;
     CUtensorMap map0, map1;
-    if (!encode_rows_map(enc, &map0, s0->X, s0->num_rows, a0.head_dim)) return HSS_ERR_CUDA;
+    if (!rows_map(enc, &map0, s0->X, s0->num_rows, a0.head_dim)) return HSS_ERR_CUDA;
     if (s1 != nullptr) {
-        if (!encode_rows_map(enc, &map1, s1->X, s1->num_rows, a0.head_dim)) return HSS_ERR_CUDA;
+        if (!rows_map(enc, &map1, s1->X, s1->num_rows, a0.head_dim)) return HSS_ERR_CUDA;
     } else {
         map1 = map0;
     }

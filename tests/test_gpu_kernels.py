@@ -315,3 +315,12 @@ def test_decode_and_tcgen05_paths_agree():
                                        offs.cpu().numpy().astype(np.int64), nthreads=8)
     for sc in out:
         assert_scores_close(sc.cpu().numpy(), ref, tsum)
+
+
+def test_binding_uses_the_current_stream():
+    # The binding reads the current stream's raw handle; it must be torch's current stream,
+    # on the default stream and inside a stream context.
+    assert hss._stream(None) == torch.cuda.current_stream().cuda_stream
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        assert hss._stream(None) == s.cuda_stream
