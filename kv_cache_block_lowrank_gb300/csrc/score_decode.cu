@@ -171,11 +171,18 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
             }
         }
     };
-    auto find_seq = [&](int64_t i) {  // the last s with seq_offsets[s] <= i
-        int lo = 0, hi = p.num_seqs;
+    // The last s with seq_offsets[s] <= i, searched 32 ways at a time: each round the lanes
+    // load 32 evenly spaced offsets of the range at once (one L2 round trip for up to 32
+    // sequences, two for up to 1024).  Whole warp.
+    auto find_seq = [&](int64_t i) {
+        int lo = 0, hi = p.num_seqs;  // seq_offsets[lo] <= i; the answer is below hi
         while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (static_cast<int64_t>(__ldg(&p.seq_offsets[mid])) <= i) lo = mid; else hi = mid;
+            const int step = (hi - lo + 31) >> 5;
+            const int j = lo + lane * step;
+            const bool le = j < hi && static_cast<int64_t>(__ldg(&p.seq_offsets[j])) <= i;
+            const unsigned below = __ballot_sync(0xffffffffu, le);  // a prefix of the lanes
+            lo += (31 - __clz(below)) * step;
+            hi = min(hi, lo + step);
         }
         return lo;
     };
@@ -188,13 +195,15 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
         // The previous kernel in the stream is this call's own projection, which writes only
         // Qp and the slots of new_ids: the offsets, the table and every other slot may be
         // read before the dependency wait, so the first block's DRAM latency overlaps it.
-        s = find_seq(i_begin);
-        seq_end = __ldg(&p.seq_offsets[s + 1]);
         const int64_t first_n = i_end - i_begin < 32 ? i_end - i_begin : 32;
         my_id = lane < first_n ? __ldg(&p.table[i_begin + lane]) : 0;
+        // num_new <= 64: two new ids per lane, loaded alongside the table entries.
+        const int32_t nid0 = lane < p.num_new ? __ldg(&p.new_ids[lane]) : -1;
+        const int32_t nid1 = lane + 32 < p.num_new ? __ldg(&p.new_ids[lane + 32]) : -1;
+        s = find_seq(i_begin);
+        seq_end = __ldg(&p.seq_offsets[s + 1]);
         const int32_t id0 = __shfl_sync(0xffffffffu, my_id, 0);
-        bool fresh = false;
-        for (int j = 0; j < p.num_new; ++j) fresh |= __ldg(&p.new_ids[j]) == id0;
+        const bool fresh = __any_sync(0xffffffffu, nid0 == id0 || nid1 == id0);
         if (id0 >= 0 && id0 < p.max_blocks && !fresh) {
             issue_loads(p.A_g + (p.layer_slots + id0) * slot_elems, 0);
             preloaded = true;
@@ -212,10 +221,10 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
         // covers it (without this call's own projection before the scorer they could not be
         // issued before the dependency wait).
         if (has_work && !preloaded) {
-            s = find_seq(i_begin);
-            seq_end = __ldg(&p.seq_offsets[s + 1]);
             const int64_t first_n = i_end - i_begin < 32 ? i_end - i_begin : 32;
             my_id = lane < first_n ? __ldg(&p.table[i_begin + lane]) : 0;
+            s = find_seq(i_begin);
+            seq_end = __ldg(&p.seq_offsets[s + 1]);
             const int32_t id0 = __shfl_sync(0xffffffffu, my_id, 0);
             if (id0 >= 0 && id0 < p.max_blocks && !__any_sync(0xffffffffu, my_new == id0)) {
                 issue_loads(p.A_g + (p.layer_slots + id0) * slot_elems, 0);
@@ -236,22 +245,42 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
         const int M = p.rows * p.nq;
         for (int z = threadIdx.x; z < p.cache_bytes / 16; z += blockDim.x)
             reinterpret_cast<uint4*>(smem_dec)[z] = make_uint4(0u, 0u, 0u, 0u);
-        const int pvec = p.r >> 3;  // 16-byte pieces per row of P
-        for (int e = threadIdx.x; e < p.hd * pvec; e += blockDim.x) {
-            const int dd = e / pvec, jc = e - dd * pvec;
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.P + dd * p.r) + jc);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            const int base = ((jc * lchunks + (dd >> 5)) * 32 + ((dd & 31) >> 3)) * 8 + (dd & 7);
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj)  // column 8 jc + jj sits in lane group jj
-                pfrag_h[base + jj * 32] = static_cast<uint16_t>(w[jj >> 1] >> ((jj & 1) * 16));
-        }
+        // Q's rows go to shared memory by asynchronous copies (no registers); P's 16-byte
+        // pieces are loaded two per thread before either is scattered, so the staging costs
+        // one L2 round trip when the pieces are at most two per thread.
         const int qvec = p.hd >> 3;
         for (int e = threadIdx.x; e < p.num_seqs * M * qvec; e += blockDim.x) {
             const int row = e / qvec, c8 = e - row * qvec;
-            reinterpret_cast<uint4*>(qs + row * qstride)[c8] = __ldg(
-                reinterpret_cast<const uint4*>(p.Q + static_cast<int64_t>(row) * p.hd) + c8);
+            cp_async_16(qs + row * qstride + 8 * c8, p.Q + static_cast<int64_t>(row) * p.hd + 8 * c8);
         }
+        const int pvec = p.r >> 3;  // 16-byte pieces per row of P: 2, 4, 8 or 16
+        const int pshift = __ffs(pvec) - 1;
+        const int p_items = p.hd * pvec;
+        for (int e0 = threadIdx.x; e0 < p_items; e0 += 2 * static_cast<int>(blockDim.x)) {
+            uint4 v[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int e = e0 + u * static_cast<int>(blockDim.x);
+                const int dd = e >> pshift, jc = e & (pvec - 1);
+                v[u] = e < p_items ? __ldg(reinterpret_cast<const uint4*>(p.P + dd * p.r) + jc)
+                                   : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int e = e0 + u * static_cast<int>(blockDim.x);
+                if (e < p_items) {
+                    const int dd = e >> pshift, jc = e & (pvec - 1);
+                    const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                    const int base =
+                        ((jc * lchunks + (dd >> 5)) * 32 + ((dd & 31) >> 3)) * 8 + (dd & 7);
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj)  // column 8 jc + jj sits in lane group jj
+                        pfrag_h[base + jj * 32] =
+                            static_cast<uint16_t>(w[jj >> 1] >> ((jj & 1) * 16));
+                }
+            }
+        }
+        cp_async_wait_all();
         __syncthreads();
         // Tasks: (sequence, 16 query vectors m, 8 columns j of r).  Vector m = row * nq + h
         // (Q's own row order); D[m][j] = sum_d Q[m][d] P[d][j] in fp32, rounded to bf16 once,
@@ -318,11 +347,16 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
     }
 
     // Column validity of this lane's accumulator entries (query vector index < nvec).
+    // Masked kernels: the query row of each of those entries (vector / g), computed once.
     bool col_ok[NT][2];
+    int col_row[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        col_ok[nt][0] = nt * 8 + 2 * tq < p.nvec;
-        col_ok[nt][1] = nt * 8 + 2 * tq + 1 < p.nvec;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+            col_ok[nt][cc] = nt * 8 + 2 * tq + cc < p.nvec;
+            col_row[nt][cc] = MASKED ? (nt * 8 + 2 * tq + cc) / p.g : 0;
+        }
     }
 
     for (int64_t i0 = i_begin; i0 < i_end; i0 += 32) {
@@ -362,86 +396,115 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
                     cache = frag_cache_all + s * frag_per_warp;  // the CTA's projection
                     cached_seq = s;
                 } else if (s != cached_seq) {
+                    // Fragment (c, ks, nt) is entry (c * KSTEPS + ks) * NT + nt; 8 per lane are
+                    // loaded before any is stored, so the refill costs one L2 round trip per
+                    // 8 fragments (not one per kv head).
+                    constexpr int kBatch = 8;
+                    const int nfrag = p.nkv * KSTEPS * NT;
                     __syncwarp();
-                    for (int c = 0; c < p.nkv; ++c) {
+                    for (int f0 = 0; f0 < nfrag; f0 += kBatch) {
+                        uint2 f[kBatch];
 #pragma unroll
-                        for (int ks = 0; ks < KSTEPS; ++ks) {
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt) {
-                                const int v = nt * 8 + gq;
-                                uint2 f = make_uint2(0u, 0u);
-                                if (v < p.nvec) {
-                                    const int row = v / p.g;
-                                    const int h = c * p.g + (v - row * p.g);
-                                    const uint16_t* q =
-                                        p.Qp +
-                                        ((static_cast<int64_t>(s) * p.rows + row) * p.nq + h) * p.r;
-                                    f = *reinterpret_cast<const uint2*>(
-                                        q + frag_r_offset<KSTEPS>(ks, tq));
-                                }
-                                cache[((c * KSTEPS + ks) * NT + nt) * 32 + lane] = f;
+                        for (int u = 0; u < kBatch; ++u) {
+                            const int fi = f0 + u;
+                            const int nt = fi % NT, ks = (fi / NT) % KSTEPS;
+                            const int c = fi / (NT * KSTEPS);
+                            const int v = nt * 8 + gq;
+                            f[u] = make_uint2(0u, 0u);
+                            if (fi < nfrag && v < p.nvec) {
+                                const int row = v / p.g;
+                                const int h = c * p.g + (v - row * p.g);
+                                const uint16_t* q =
+                                    p.Qp + ((static_cast<int64_t>(s) * p.rows + row) * p.nq + h) *
+                                               p.r;
+                                f[u] = *reinterpret_cast<const uint2*>(
+                                    q + frag_r_offset<KSTEPS>(ks, tq));
                             }
                         }
+#pragma unroll
+                        for (int u = 0; u < kBatch; ++u)
+                            if (f0 + u < nfrag) cache[(f0 + u) * 32 + lane] = f[u];
                     }
                     __syncwarp();
                     cached_seq = s;
                 }
+                // One 16-token tile: the MMAs over r for kv head c, then the max into `best`.
+                auto score_tile = [&](const int u, const int c, const int in_head) {
+                    float acc[NT][4];
 #pragma unroll
-                for (int u = 0; u < kTilesPerBatch; ++u) {
-                    const int tile = tb + u;
-                    if (tile < num_tiles) {
-                        const int c = tile / tiles_per_head;
-                        float acc[NT][4];
+                    for (int nt = 0; nt < NT; ++nt)
+                        acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-#pragma unroll
-                        for (int ks = 0; ks < KSTEPS; ++ks) {
-                            uint32_t a0, a1, a2, a3;
-                            if constexpr (KSTEPS == 1) {
-                                a0 = data[u][0];  // token row gq,     r 4t..4t+1
-                                a2 = data[u][1];  // token row gq,     r 4t+2..4t+3
-                                a1 = data[u][2];  // token row gq + 8
-                                a3 = data[u][3];
-                            } else {
-                                const int l = ks >> 1, w = ks & 1;
-                                a0 = data[u][(0 * kLoadsPerRow + l) * 4 + 2 * w + 0];
-                                a2 = data[u][(0 * kLoadsPerRow + l) * 4 + 2 * w + 1];
-                                a1 = data[u][(1 * kLoadsPerRow + l) * 4 + 2 * w + 0];
-                                a3 = data[u][(1 * kLoadsPerRow + l) * 4 + 2 * w + 1];
-                            }
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt) {
-                                const uint2 b = cache[((c * KSTEPS + ks) * NT + nt) * 32 + lane];
-                                mma_bf16_16816(acc[nt], a0, a1, a2, a3, b.x, b.y);
-                            }
-                        }
-                        if (!MASKED) {
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt) {
-                                if (col_ok[nt][0])
-                                    best = fmaxf(best, fmaxf(acc[nt][0], acc[nt][2]));
-                                if (col_ok[nt][1])
-                                    best = fmaxf(best, fmaxf(acc[nt][1], acc[nt][3]));
-                            }
+                    for (int ks = 0; ks < KSTEPS; ++ks) {
+                        uint32_t a0, a1, a2, a3;
+                        if constexpr (KSTEPS == 1) {
+                            a0 = data[u][0];  // token row gq,     r 4t..4t+1
+                            a2 = data[u][1];  // token row gq,     r 4t+2..4t+3
+                            a1 = data[u][2];  // token row gq + 8
+                            a3 = data[u][3];
                         } else {
-                            // Accumulator rows are tokens gq and gq + 8 of this 16-token tile,
-                            // columns are query vectors (row = vector / g).
-                            const int mt = tile - c * tiles_per_head;
-                            const int64_t p_lo = (i - seq_begin) * p.bs + mt * 16 + gq;
-                            const int64_t p_hi = p_lo + 8;
+                            const int l = ks >> 1, w = ks & 1;
+                            a0 = data[u][(0 * kLoadsPerRow + l) * 4 + 2 * w + 0];
+                            a2 = data[u][(0 * kLoadsPerRow + l) * 4 + 2 * w + 1];
+                            a1 = data[u][(1 * kLoadsPerRow + l) * 4 + 2 * w + 0];
+                            a3 = data[u][(1 * kLoadsPerRow + l) * 4 + 2 * w + 1];
+                        }
 #pragma unroll
-                            for (int nt = 0; nt < NT; ++nt) {
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const uint2 b = cache[((c * KSTEPS + ks) * NT + nt) * 32 + lane];
+                            mma_bf16_16816(acc[nt], a0, a1, a2, a3, b.x, b.y);
+                        }
+                    }
+                    if (!MASKED) {
 #pragma unroll
-                                for (int cc = 0; cc < 2; ++cc) {
-                                    if (!col_ok[nt][cc]) continue;
-                                    const int64_t lim = min(clen - 1,
-                                                            pos0 + (nt * 8 + 2 * tq + cc) / p.g);
-                                    if (p_lo <= lim) best = fmaxf(best, acc[nt][cc]);
-                                    if (p_hi <= lim) best = fmaxf(best, acc[nt][cc + 2]);
-                                }
+                        for (int nt = 0; nt < NT; ++nt) {
+                            best = fmaxf(best, col_ok[nt][0] ? fmaxf(acc[nt][0], acc[nt][2])
+                                                             : -INFINITY);
+                            best = fmaxf(best, col_ok[nt][1] ? fmaxf(acc[nt][1], acc[nt][3])
+                                                             : -INFINITY);
+                        }
+                    } else {
+                        // Accumulator rows are tokens gq and gq + 8 of this 16-token tile,
+                        // columns are query vectors (row = vector / g).
+                        const int64_t p_lo = (i - seq_begin) * p.bs + in_head * 16 + gq;
+                        const int64_t p_hi = p_lo + 8;
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                            for (int cc = 0; cc < 2; ++cc) {
+                                if (!col_ok[nt][cc]) continue;
+                                const int64_t lim = min(clen - 1, pos0 + col_row[nt][cc]);
+                                if (p_lo <= lim) best = fmaxf(best, acc[nt][cc]);
+                                if (p_hi <= lim) best = fmaxf(best, acc[nt][cc + 2]);
                             }
                         }
+                    }
+                };
+                // kv head c of the batch's first tile and the tile's place in its head, then
+                // stepped tile by tile with selects.  A division, or a branch around each tile,
+                // in the unrolled bodies below would serialise them: each tile's fragment
+                // loads and MMAs would wait for the one before (measured: 5x the arithmetic
+                // time of a block).  Only a batch that runs past the last tile tests each tile.
+                int c = 0, in_head = 0;
+                if (tb != 0) {
+                    c = tb / tiles_per_head;
+                    in_head = tb - c * tiles_per_head;
+                }
+                if (tb + kTilesPerBatch <= num_tiles) {
+#pragma unroll
+                    for (int u = 0; u < kTilesPerBatch; ++u) {
+                        score_tile(u, c, in_head);
+                        const bool wrap = in_head + 1 == tiles_per_head;
+                        in_head = wrap ? 0 : in_head + 1;
+                        c += wrap ? 1 : 0;
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < kTilesPerBatch; ++u) {
+                        if (tb + u < num_tiles) score_tile(u, c, in_head);
+                        const bool wrap = in_head + 1 == tiles_per_head;
+                        in_head = wrap ? 0 : in_head + 1;
+                        c += wrap ? 1 : 0;
                     }
                 }
             }
