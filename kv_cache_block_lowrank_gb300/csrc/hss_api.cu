@@ -246,8 +246,10 @@ hss_status hss_rank_victims(const float* scores, const int32_t* seq_offsets, int
 
 size_t hss_layer_step_workspace_bytes(int32_t num_seqs) {
     if (num_seqs <= 0) return 0;
+    // Per-sequence completion counters (rounded up to 256 bytes), then the two counters of the
+    // one-sequence spread ranking, one per 128-byte line.
     const size_t b = static_cast<size_t>(num_seqs) * sizeof(int32_t);
-    return (b + 255) / 256 * 256;
+    return (b + 255) / 256 * 256 + 256;
 }
 
 hss_status hss_layer_step(const hss_dims* dims, const uint16_t* P, const uint16_t* K_new,

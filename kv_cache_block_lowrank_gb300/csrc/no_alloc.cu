@@ -9,8 +9,8 @@
 // that is part of the library itself, so the call needs nothing beyond its inputs and
 // outputs.
 //
-// The array holds the counters of at most kStaticMaxSeqs sequences (16 KiB on each GPU that
-// loads the library, held until the process exits).  Every call shares it, so calls that
+// The array holds the counters of at most kStaticMaxSeqs sequences and 256 bytes of grid-wide
+// counters (16.25 KiB on each GPU that loads the library, held until the process exits).  Every call shares it, so calls that
 // overlap on the GPU (on different streams, or on one stream without ordering) race.
 #include <mutex>
 
@@ -21,7 +21,8 @@ namespace {
 
 constexpr int kStaticMaxSeqs = HSS_LAYER_STEP_STATIC_MAX_SEQS;
 
-static __device__ __align__(256) int32_t g_static_counters[kStaticMaxSeqs];
+constexpr int kStaticWords = kStaticMaxSeqs + 64;
+static __device__ __align__(256) int32_t g_static_counters[kStaticWords];
 
 // Device address of g_static_counters, looked up once per device with that device current
 // (the symbol's name in host code is only a stand-in, not an address a kernel can use).
@@ -87,12 +88,12 @@ hss_status hss_layer_step_static(const hss_dims* dims, const uint16_t* P, const 
     // The counters must start at zero.  A completed call leaves them zero, but the array
     // outlives every call (and an earlier call may have stopped early), so clear the part
     // this call uses, in stream order.
-    if (cudaMemsetAsync(counters, 0, static_cast<size_t>(num_seqs) * sizeof(int32_t),
+    if (cudaMemsetAsync(counters, 0, hss_layer_step_workspace_bytes(num_seqs),
                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return HSS_ERR_CUDA;
     return hss_layer_step(dims, P, K_new, new_ids, num_new, Q, rows_per_seq, Qp, A_g, layer,
                           block_table, seq_offsets, num_seqs, total_blocks, scores, k, victims,
-                          counters, static_cast<size_t>(kStaticMaxSeqs) * sizeof(int32_t),
+                          counters, static_cast<size_t>(kStaticWords) * sizeof(int32_t),
                           dev_status, stream);
 }
 

@@ -21,6 +21,7 @@
 //   * the max over tokens and query vectors is reduced in registers, then across the warp
 //     with shuffles; padded query-vector columns are masked to -inf.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
 #include "rank_device.cuh"
@@ -85,7 +86,66 @@ struct DecodeParams {
     // of the new_ids slots and nothing else, so only a warp about to read one of those slots
     // takes the grid dependency wait; num_new <= 32 then.
     int32_t nowait;
+    // spread != 0 (one sequence of at most kSpreadMaxEntries entries, every CTA of the grid
+    // resident at once): instead of the last CTA ranking the whole sequence, every CTA waits
+    // until the sequence's count is complete and places its own entries by counting the
+    // smaller words, so the ranking is spread over the grid.
+    int32_t spread;
 };
+
+// Spread ranking: keys per thread (256 threads) and so the longest sequence it takes.
+constexpr int kSpreadKeysPerThread = 16;
+constexpr int kSpreadMaxEntries = kWarpsMax * 32 * kSpreadKeysPerThread;
+// ... and the most entries one CTA scores and places (2 per warp at 4096 entries on 152 SMs).
+constexpr int kSpreadMaxCta = 16;
+// Its two counters (arrivals, departures) sit after the one sequence's counter, 256 bytes into
+// the workspace, in lines of their own.
+constexpr int kSpreadRegionWords = 64;
+
+__device__ __forceinline__ void red_add_release_gpu(int* addr, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_add_relaxed_gpu(int* addr, int v) {
+    asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* addr) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+    return v;
+}
+
+// below -= [w < we] for 64-bit unsigned words: one borrow chain, no predicate or branch (a
+// compare-and-select per pair issued about twice the instructions).
+__device__ __forceinline__ void sub_if_less(uint32_t& below, uint64_t w, uint64_t we) {
+    asm("{\n\t"
+        ".reg .u32 t;\n\t"
+        "sub.cc.u32 t, %1, %3;\n\t"
+        "subc.cc.u32 t, %2, %4;\n\t"
+        "subc.u32 %0, %0, 0;\n\t"
+        "}"
+        : "+r"(below)
+        : "r"(static_cast<uint32_t>(w)), "r"(static_cast<uint32_t>(w >> 32)),
+          "r"(static_cast<uint32_t>(we)), "r"(static_cast<uint32_t>(we >> 32)));
+}
+
+// neg_below[u] -= the number of the first SLOTS words w[] below we[u].  The slot count is a
+// template parameter: a per-slot test inside the unrolled loop cost as much as the compares.
+template <int SLOTS, int N>
+__device__ __forceinline__ void count_below(const uint64_t (&w)[N], const uint64_t (&we)[4],
+                                            uint32_t (&neg_below)[4]) {
+#pragma unroll
+    for (int q = 0; q < SLOTS; ++q)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) sub_if_less(neg_below[u], w[q], we[u]);
+}
+
+__device__ __forceinline__ int ld_relaxed_gpu(const int* addr) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+    return v;
+}
 
 __device__ __forceinline__ int atom_add_acq_rel_gpu(int* addr, int v) {
     int old;
@@ -211,7 +271,9 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
     }
     const bool nowait = INLINE && p.nowait != 0;
     if (!nowait) grid_dependency_wait();
-    grid_launch_dependents();
+    // Spread ranking waits for every CTA of this grid: the next kernel may not take their
+    // places (it is let in once all of them have arrived).
+    if (!p.spread) grid_launch_dependents();
     // nowait: this lane's new id (lane < num_new <= 32); a warp waits before its first one.
     const int32_t my_new = nowait && lane < p.num_new ? __ldg(&p.new_ids[lane]) : -1;
     bool waited = !nowait;
@@ -517,6 +579,108 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
     }  // has_work
     if (p.counters == nullptr) return;
 
+    if (p.spread) {
+        // ---- spread ranking of the one sequence [a, b): the rank of entry e is the number
+        // of words (key << 32 | position) below its own; entry e is victim number rank(e)
+        // when that is below k.  The words are unique, so the ranks are a permutation.
+        uint32_t* ekey = reinterpret_cast<uint32_t*>(smem_dec + p.frag_bytes_cta);
+        uint32_t* part = ekey + p.todo_cap;  // [warp][kSpreadMaxCta] partial counts
+        const int64_t per_cta = p.entries_per_warp * (blockDim.x >> 5);
+        const int64_t cb = static_cast<int64_t>(blockIdx.x) * per_cta;
+        // (loaded before the barrier: the latency overlaps the CTA's slowest warp)
+        const int64_t a = __ldg(&p.seq_offsets[0]), b = __ldg(&p.seq_offsets[1]);
+        const int64_t eb = max(cb, a), ee = min(min(p.total, cb + per_cta), b);
+        const int cnt = ee > eb ? static_cast<int>(ee - eb) : 0;  // <= kSpreadMaxCta
+        const int n = static_cast<int>(min(b, p.total) - a);  // entries the counts reach
+        // Arrive: the barrier orders every warp's scores before thread 0's count, a release
+        // at GPU scope (no reply is awaited).  The additions form one release sequence, so
+        // the acquire load that sees the count complete sees every other CTA's scores.
+        int* arrive = p.counters + kSpreadRegionWords;
+        int* depart = arrive + 32;
+        __syncthreads();
+        if (threadIdx.x == 0 && cnt > 0) {
+            red_add_release_gpu(arrive, cnt);
+            const uint64_t t0 = global_timer_ns();
+            while (ld_acquire_gpu(arrive) < n) {
+                if (global_timer_ns() - t0 > kWaitLimitNs) {
+                    raise_error(p.dev_status, p.lib_error, HSS_ERR_DEVICE_TIMEOUT);
+                    break;
+                }
+            }
+        }
+        __syncthreads();
+        grid_launch_dependents();
+        // Words of the sequence (16 per thread; past the end a word above every real one:
+        // NaN and +inf map to key 0xFF800000) and this CTA's own entries' keys.
+        uint64_t w[kSpreadKeysPerThread];
+#pragma unroll
+        for (int q = 0; q < kSpreadKeysPerThread; ++q) {
+            const int j = static_cast<int>(threadIdx.x) + q * kWarpsMax * 32;
+            w[q] = j < n ? (static_cast<uint64_t>(
+                                rankdev::rank_key<false>(__ldcg(&p.scores[a + j])))
+                            << 32) | static_cast<uint32_t>(j)
+                         : ~0ull;
+        }
+        if (static_cast<int>(threadIdx.x) < cnt)
+            ekey[threadIdx.x] = rankdev::rank_key<false>(__ldcg(&p.scores[eb + threadIdx.x]));
+        __syncthreads();
+        // Depart: this CTA reads no counter and no other CTA's score from here on.
+        if (threadIdx.x == 0 && cnt > 0) red_add_relaxed_gpu(depart, 1);
+        const int pos0 = static_cast<int>(eb - a);  // position of this CTA's first entry
+        // Four entries at a time; each warp leaves its four totals in `part`, lane u writing
+        // entry e0 + u (no atomics, no branch per entry).  Slots past the sequence hold a word
+        // above every real one, so half the slots are skipped whole when n <= 2048.
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        for (int e0 = 0; e0 < cnt; e0 += 4) {
+            uint64_t we[4];
+            uint32_t neg[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                we[u] = e0 + u < cnt ? (static_cast<uint64_t>(ekey[e0 + u]) << 32) |
+                                           static_cast<uint32_t>(pos0 + e0 + u)
+                                     : 0ull;
+                neg[u] = 0;
+            }
+            if (n <= kSpreadKeysPerThread / 2 * kWarpsMax * 32)
+                count_below<kSpreadKeysPerThread / 2>(w, we, neg);
+            else
+                count_below<kSpreadKeysPerThread>(w, we, neg);
+            uint32_t tot[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) tot[u] = __reduce_add_sync(0xffffffffu, 0u - neg[u]);
+            const uint32_t mine = lane == 0 ? tot[0] : lane == 1 ? tot[1] : lane == 2 ? tot[2]
+                                                                               : tot[3];
+            if (lane < 4 && e0 + lane < cnt) part[warp * kSpreadMaxCta + e0 + lane] = mine;
+        }
+        __syncthreads();
+        if (static_cast<int>(threadIdx.x) < cnt) {
+            uint32_t rank = 0;
+#pragma unroll
+            for (int wv = 0; wv < kWarpsMax; ++wv) rank += part[wv * kSpreadMaxCta + threadIdx.x];
+            if (rank < static_cast<uint32_t>(p.k))
+                p.victims[rank] = pos0 + static_cast<int>(threadIdx.x);
+        }
+        if (blockIdx.x == 0)
+            for (int j = n + static_cast<int>(threadIdx.x); j < p.k; j += blockDim.x)
+                p.victims[j] = -1;
+        // The sequence's first CTA clears the counters for the next call once every CTA that
+        // arrived has departed (none of them reads a counter again).
+        if (threadIdx.x == 0 && n > 0 && static_cast<int64_t>(blockIdx.x) == a / per_cta) {
+            const int64_t last_entry = min(p.total, b) - 1;
+            const int ctas = static_cast<int>(last_entry / per_cta - a / per_cta) + 1;
+            const uint64_t t0 = global_timer_ns();
+            while (ld_relaxed_gpu(depart) < ctas) {
+                if (global_timer_ns() - t0 > kWaitLimitNs) {
+                    raise_error(p.dev_status, p.lib_error, HSS_ERR_DEVICE_TIMEOUT);
+                    break;
+                }
+            }
+            *arrive = 0;
+            *depart = 0;
+        }
+        return;
+    }
+
     // ---- fused ranking: the CTA that completes a sequence ranks it
     constexpr int kThreadsFused = kWarpsMax * 32;
     uint8_t* rank_smem = smem_dec + p.frag_bytes_cta;
@@ -571,12 +735,38 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
 }
 
 template <int KSTEPS, int NT>
+auto kernel_for(const DecodeParams& p) {
+    const bool masked = p.ctx_len != nullptr || p.row_pos0 != nullptr;
+    return p.Q != nullptr ? score_decode_kernel<KSTEPS, NT, false, true>
+           : masked       ? score_decode_kernel<KSTEPS, NT, true, false>
+                          : score_decode_kernel<KSTEPS, NT, false, false>;
+}
+
+// CTAs of 256 threads with `smem` bytes of dynamic shared memory that one SM holds at once,
+// for the kernel `p` selects (cached per kernel: the last shared-memory size asked for).
+template <int KSTEPS, int NT>
+int ctas_per_sm_t(const DecodeParams& p, int smem) {
+    static std::atomic<uint64_t> cache[3];  // (smem << 32 | ctas) per kernel of kernel_for
+    const int which = p.Q != nullptr ? 0 : (p.ctx_len != nullptr || p.row_pos0 != nullptr) ? 1 : 2;
+    const uint64_t c = cache[which].load(std::memory_order_relaxed);
+    if (c != 0 && static_cast<int>(c >> 32) == smem) return static_cast<int>(c & 0xFFFFFFFFu);
+    auto k = kernel_for<KSTEPS, NT>(p);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return 0;
+    int ctas = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctas, k, kWarpsMax * 32, smem) !=
+        cudaSuccess)
+        return 0;
+    cache[which].store((static_cast<uint64_t>(smem) << 32) | static_cast<uint32_t>(ctas),
+                       std::memory_order_relaxed);
+    return ctas;
+}
+
+template <int KSTEPS, int NT>
 hss_status launch_t(const DecodeParams& p, int warps_per_cta, int smem, int grid,
                     cudaStream_t stream) {
-    const bool masked = p.ctx_len != nullptr || p.row_pos0 != nullptr;
-    auto k = p.Q != nullptr ? score_decode_kernel<KSTEPS, NT, false, true>
-             : masked       ? score_decode_kernel<KSTEPS, NT, true, false>
-                            : score_decode_kernel<KSTEPS, NT, false, false>;
+    auto k = kernel_for<KSTEPS, NT>(p);
     if (smem > 48 * 1024) {
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
             cudaSuccess)
@@ -688,7 +878,38 @@ hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream, const Fu
     // The ranking can ride along when a whole CTA of 8 warps is there to run it, every
     // sequence's keys fit in shared memory and the extra shared memory stays modest.
     // Long sequences are ranked by the dedicated kernel (1024 threads) instead.
+    const int ksteps = a.r / 16;
+    const int nt = (p.nvec + 7) / 8;
+    p.spread = 0;
     if (fr != nullptr && fr->counters != nullptr && warps_per_cta == kWarpsMax &&
+        a.num_seqs == 1 && a.total <= kSpreadMaxEntries &&
+        p.entries_per_warp * warps_per_cta <= kSpreadMaxCta) {
+        // Spread ranking needs the whole grid resident at once (its CTAs wait for each other).
+        const int todo_cap = static_cast<int>(p.entries_per_warp * warps_per_cta);
+        const int smem_spread = smem + 4 * todo_cap + 4 * kWarpsMax * kSpreadMaxCta;
+        int per_sm = 0;
+#define HSS_DECODE_CASE(KS, NT_) \
+    if (ksteps == KS && nt == NT_) per_sm = ctas_per_sm_t<KS, NT_>(p, smem_spread);
+        HSS_DECODE_CASE(1, 1)
+        HSS_DECODE_CASE(1, 2)
+        HSS_DECODE_CASE(2, 1)
+        HSS_DECODE_CASE(2, 2)
+        HSS_DECODE_CASE(4, 1)
+        HSS_DECODE_CASE(4, 2)
+        HSS_DECODE_CASE(8, 1)
+        HSS_DECODE_CASE(8, 2)
+#undef HSS_DECODE_CASE
+        if (static_cast<int64_t>(per_sm) * dev->num_sms >= grid) {
+            p.spread = 1;
+            p.todo_cap = todo_cap;
+            p.counters = fr->counters;
+            p.victims = fr->victims;
+            p.k = fr->k;
+            smem = smem_spread;
+            if (fused != nullptr) *fused = true;
+        }
+    }
+    if (!p.spread && fr != nullptr && fr->counters != nullptr && warps_per_cta == kWarpsMax &&
         a.total <= kWarpsMax * 32 * rankdev::keys_per_thread<kWarpsMax * 32>()) {
         const int sel_cap = rankdev::rank_sel_cap(fr->k);
         const int todo_cap = static_cast<int>(p.entries_per_warp * warps_per_cta);
@@ -704,8 +925,6 @@ hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream, const Fu
         }
     }
 
-    const int ksteps = a.r / 16;
-    const int nt = (p.nvec + 7) / 8;
 #define HSS_DECODE_CASE(KS, NT_)                                                        \
     if (ksteps == KS && nt == NT_) return launch_t<KS, NT_>(p, warps_per_cta, smem, grid, stream);
     HSS_DECODE_CASE(1, 1)

@@ -101,10 +101,11 @@ def test_layer_step_against_oracle():
     Qp = torch.empty(1, 1, d.num_q_heads, d.r, dtype=torch.bfloat16, device=DEV)
     sc = torch.empty(64, dtype=torch.float32, device=DEV)
     vic = torch.empty(1, 8, dtype=torch.int32, device=DEV)
-    ws = torch.zeros(64, dtype=torch.int32, device=DEV)
+    nb = hss.hss_layer_step_workspace_bytes(1)
+    ws = torch.zeros(nb // 4, dtype=torch.int32, device=DEV)
     table, offs = case.table.to(DEV), case.seq_offsets.to(DEV)
     hss.hss_layer_step(d, P, case.K[0][60:].to(DEV), new_ids, 4, case.Q[0].to(DEV), 1, Qp, A, 0,
-                       table, offs, 1, 64, sc, 8, vic, ws, 256)
+                       table, offs, 1, 64, sc, 8, vic, ws, nb)
     torch.cuda.synchronize()
     A_o = np.zeros(d.a_g_shape, dtype=np.uint16)
     oracle.project_kv_blocks(bits(case.P), bits(case.K[0]), 0, case.block_ids.numpy(), A_o)
@@ -167,3 +168,96 @@ def test_layer_step_inline_new_block_outside_the_table():
     outside = next(b for b in range(d.max_blocks) if b not in in_table)
     x["new_ids"] = torch.tensor([int(x["table"][7]), outside], dtype=torch.int32, device=DEV)
     inline_vs_oracle(d, x, 0, 32)
+
+
+def _with_ties(x, d, groups, seed):
+    """Replace the table by `groups` distinct blocks, each named several times: equal scores,
+    which the ranking must order by table position."""
+    g = torch.Generator().manual_seed(seed)
+    total = x["total"]
+    base = torch.randperm(d.max_blocks, generator=g)[:groups].to(torch.int32)
+    table = base[torch.randint(0, groups, (total,), generator=g)]
+    x["table"] = table.to(DEV)
+    if x["n_new"]:
+        x["new_ids"] = table[:x["n_new"]].unique().contiguous().to(DEV)
+        x["n_new"] = int(x["new_ids"].numel())
+    return x
+
+
+# One sequence of at most 4096 entries: every CTA of the decode scorer ranks its own entries
+# once the sequence's count is complete.  Past 4096 the last CTA ranks the whole sequence.
+@pytest.mark.parametrize("shape,n,k,ties,inline", [
+    ((2, 32, 8, 128, 32, 16, 2100), 2048, 256, 0, True),     # the decode layer
+    ((2, 32, 8, 128, 32, 16, 2100), 2048, 256, 97, True),    # many equal scores
+    ((1, 32, 8, 128, 32, 16, 5000), 4096, 4096, 0, False),   # the longest spread sequence
+    ((1, 32, 8, 128, 32, 16, 5000), 4097, 300, 0, True),     # one entry past it
+    ((1, 32, 8, 128, 32, 16, 500), 100, 256, 0, True),       # fewer entries than victims
+    ((1, 32, 8, 128, 32, 16, 500), 1, 8, 0, False),          # a single entry
+    ((1, 8, 2, 64, 16, 16, 900), 777, 777, 5, True),         # r 16, k == n, ties
+])
+def test_layer_step_one_sequence_ranking(shape, n, k, ties, inline):
+    d = W.Dims(*shape)
+    x = make(d, [n], 1, 1, seed=n + k + ties)
+    if ties:
+        x = _with_ties(x, d, ties, seed=n)
+    layer = d.num_layers - 1
+    A1, _, sc1, vic1 = separate(d, x, layer, k)
+    A = x["A"].clone()
+    sc = torch.empty(n, dtype=torch.float32, device=DEV)
+    vic = torch.full((1, k), 12345, dtype=torch.int32, device=DEV)
+    nb = hss.hss_layer_step_workspace_bytes(1)
+    ws = torch.zeros(max(nb, 4) // 4, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    Qp = None if inline else torch.empty(1, 1, d.num_q_heads, d.r, dtype=torch.bfloat16,
+                                         device=DEV)
+    for _ in range(3):  # the workspace is reused: each call must leave it zeroed
+        vic.fill_(12345)
+        hss.hss_layer_step(d, x["P"], x["K_new"], x["new_ids"], x["n_new"], x["Q"], 1, Qp, A,
+                           layer, x["table"], x["offs"], 1, n, sc, k, vic, ws, nb, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert int(ws.abs().sum()) == 0, "the workspace must be left zeroed"
+        assert torch.equal(sc, sc1)
+        assert torch.equal(vic, vic1)
+    if ties:
+        s = sc1.cpu().numpy()
+        assert len(np.unique(s)) <= ties
+    v = vic1[0].cpu().numpy()
+    assert (v[min(n, k):] == -1).all()
+    assert sorted(v[:min(n, k)].tolist()) == sorted(set(v[:min(n, k)].tolist()))
+
+
+def test_layer_step_one_sequence_bad_id():
+    # A table entry outside the pool scores +inf and raises the status; the ranking still
+    # places it (last) exactly as the separate ranking call does.
+    d = W.Dims(1, 32, 8, 128, 32, 16, 3000)
+    n, k = 2048, 2048
+    x = make(d, [n], 1, 1, seed=5)
+    x["table"][777] = d.max_blocks + 3
+    layer = 0
+    Qp = torch.empty(1, 1, d.num_q_heads, d.r, dtype=torch.bfloat16, device=DEV)
+    A = x["A"].clone()
+    hss.hss_project_kv_blocks(d, x["P"], x["K_new"], layer, x["new_ids"], 1, A)
+    hss.hss_project_q(d, x["P"], x["Q"], 1, Qp)
+    sc1 = torch.empty(n, dtype=torch.float32, device=DEV)
+    st1 = torch.zeros(1, dtype=torch.int32, device=DEV)
+    hss.hss_score_blocks(d, Qp, 1, A, layer, x["table"], x["offs"], 1, n, sc1,
+                         dev_status=st1)
+    vic1 = torch.empty(1, k, dtype=torch.int32, device=DEV)
+    hss.hss_rank_victims(sc1, x["offs"], 1, n, k, vic1)
+    sc = torch.empty(n, dtype=torch.float32, device=DEV)
+    vic = torch.full((1, k), 12345, dtype=torch.int32, device=DEV)
+    nb = hss.hss_layer_step_workspace_bytes(1)
+    ws = torch.zeros(max(nb, 4) // 4, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    hss.hss_layer_step(d, x["P"], x["K_new"], x["new_ids"], 1, x["Q"], 1, None, x["A"].clone(),
+                       layer, x["table"], x["offs"], 1, n, sc, k, vic, ws, nb, st)
+    torch.cuda.synchronize()
+    assert int(st1.item()) == hss.HSS_ERR_OUT_OF_RANGE
+    assert int(st.item()) == hss.HSS_ERR_OUT_OF_RANGE
+    assert float(sc[777]) == float("inf")
+    assert torch.equal(sc, sc1)
+    assert torch.equal(vic, vic1)
+    assert int(vic[0, -1]) == 777
+    assert int(ws.abs().sum()) == 0
+    assert hss.hss_read_device_error() == hss.HSS_ERR_OUT_OF_RANGE
