@@ -271,9 +271,10 @@ hss_status hss_select_rows(const float* scores, int32_t rows, int64_t num_blocks
  * on the same stream (the same kernels compute them; the victims are the same words in
  * the same order).  In the decode regime the victim ranking runs inside the scoring kernel:
  * for one sequence of at most 4096 blocks whose scoring grid fits on the GPU at once, every
- * CTA waits until the sequence is scored (a bounded wait: HSS_ERR_DEVICE_TIMEOUT after 1 s)
- * and places its own blocks by counting the smaller (score, position) words; otherwise the
- * last CTA to finish a sequence ranks it.
+ * CTA publishes its blocks' keys in the workspace, waits until the sequence's keys are all
+ * there (a bounded wait: HSS_ERR_DEVICE_TIMEOUT after 1 s) and places its own blocks by
+ * counting the smaller (score, position) words; otherwise the last CTA to finish a sequence
+ * ranks it.
  * This is the fused decode call the predictor page's per-step usage implies (module docs
  * of "metrale_storage/predictor.rs": scores only rank eviction victims).
  *
@@ -297,12 +298,15 @@ hss_status hss_select_rows(const float* scores, int32_t rows, int64_t num_blocks
  *                            bf16 ulp.
  *   scores, victims          outputs, as in hss_score_blocks / hss_rank_victims
  *   workspace                device, >= hss_layer_step_workspace_bytes(num_seqs) bytes,
- *                            4-byte aligned: per-sequence completion counters, then 256 bytes
- *                            of grid-wide counters (one sequence).  Zero it once (e.g.
- *                            cudaMemsetAsync) before its first use; every call that returns
- *                            no device error leaves it zero again (after
- *                            HSS_ERR_DEVICE_TIMEOUT, zero it again).  Two calls that share a
- *                            workspace must not run at the same time on the GPU.
+ *                            4-byte aligned (8-byte aligned for the one-sequence ranking
+ *                            above): per-sequence completion counters, then a call number
+ *                            and 32 KiB of tagged keys for one sequence.  Zero all of it once
+ *                            (e.g. cudaMemsetAsync) before its first use, then leave it as
+ *                            each call leaves it: the counters return to zero, the call
+ *                            number and the keys carry over to the next call (zeroing all
+ *                            of it again is also fine; after HSS_ERR_DEVICE_TIMEOUT, do).
+ *                            Two calls that share a workspace must not run at the same time
+ *                            on the GPU.
  * Errors as in the four calls above; HSS_ERR_WORKSPACE_TOO_SMALL if the workspace is short.
  */
 size_t hss_layer_step_workspace_bytes(int32_t num_seqs);
@@ -324,7 +328,7 @@ hss_status hss_layer_step(const hss_dims* dims, const uint16_t* P, const uint16_
  * start-up, a library hosted by a process that hands it no allocator, or a caller that only
  * holds raw pointers to its own buffers.  This variant takes no workspace: the completion
  * counters live in a fixed array inside the library, HSS_LAYER_STEP_STATIC_MAX_SEQS int32
- * words and 256 bytes more (16.25 KiB) on every GPU that loads it, kept until the process
+ * words and 32.25 KiB more (48.25 KiB) on every GPU that loads it, kept until the process
  * exits.  It allocates
  * nothing and calls no allocating routine.
  *

@@ -246,10 +246,11 @@ hss_status hss_rank_victims(const float* scores, const int32_t* seq_offsets, int
 
 size_t hss_layer_step_workspace_bytes(int32_t num_seqs) {
     if (num_seqs <= 0) return 0;
-    // Per-sequence completion counters (rounded up to 256 bytes), then the two counters of the
-    // one-sequence spread ranking, one per 128-byte line.
+    // Per-sequence completion counters (rounded up to 256 bytes), then the one-sequence spread
+    // ranking's call number (256 bytes) and its tagged words (8 bytes for each of at most
+    // 4096 entries).
     const size_t b = static_cast<size_t>(num_seqs) * sizeof(int32_t);
-    return (b + 255) / 256 * 256 + 256;
+    return (b + 255) / 256 * 256 + 256 + 8 * 4096;
 }
 
 hss_status hss_layer_step(const hss_dims* dims, const uint16_t* P, const uint16_t* K_new,

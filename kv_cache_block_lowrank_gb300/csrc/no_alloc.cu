@@ -9,8 +9,9 @@
 // that is part of the library itself, so the call needs nothing beyond its inputs and
 // outputs.
 //
-// The array holds the counters of at most kStaticMaxSeqs sequences and 256 bytes of grid-wide
-// counters (16.25 KiB on each GPU that loads the library, held until the process exits).  Every call shares it, so calls that
+// The array holds the counters of at most kStaticMaxSeqs sequences and the one-sequence
+// ranking's 32.25 KiB (48.25 KiB on each GPU that loads the library, held until the process
+// exits).  Every call shares it, so calls that
 // overlap on the GPU (on different streams, or on one stream without ordering) race.
 #include <mutex>
 
@@ -21,7 +22,7 @@ namespace {
 
 constexpr int kStaticMaxSeqs = HSS_LAYER_STEP_STATIC_MAX_SEQS;
 
-constexpr int kStaticWords = kStaticMaxSeqs + 64;
+constexpr int kStaticWords = kStaticMaxSeqs + 64 + 2 * 4096;
 static __device__ __align__(256) int32_t g_static_counters[kStaticWords];
 
 // Device address of g_static_counters, looked up once per device with that device current

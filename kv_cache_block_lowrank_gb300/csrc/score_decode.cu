@@ -98,23 +98,10 @@ constexpr int kSpreadKeysPerThread = 16;
 constexpr int kSpreadMaxEntries = kWarpsMax * 32 * kSpreadKeysPerThread;
 // ... and the most entries one CTA scores and places (2 per warp at 4096 entries on 152 SMs).
 constexpr int kSpreadMaxCta = 16;
-// Its two counters (arrivals, departures) sit after the one sequence's counter, 256 bytes into
-// the workspace, in lines of their own.
+// Its workspace region follows the one sequence's counter (256 bytes in): the call number (a
+// line of its own), then from byte 512 one tagged word per entry (32 KiB).
 constexpr int kSpreadRegionWords = 64;
-
-__device__ __forceinline__ void red_add_release_gpu(int* addr, int v) {
-    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void red_add_relaxed_gpu(int* addr, int v) {
-    asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ int ld_acquire_gpu(const int* addr) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
-    return v;
-}
+constexpr int kSpreadWordsOffsetWords = 128;
 
 // below -= [w < we] for 64-bit unsigned words: one borrow chain, no predicate or branch (a
 // compare-and-select per pair issued about twice the instructions).
@@ -145,6 +132,20 @@ __device__ __forceinline__ int ld_relaxed_gpu(const int* addr) {
     int v;
     asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
     return v;
+}
+
+__device__ __forceinline__ uint64_t ld_relaxed_gpu_u64(const uint64_t* addr) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu_u64(uint64_t* addr, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(addr), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_gpu_s32(int* addr, int v) {
+    asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ int atom_add_acq_rel_gpu(int* addr, int v) {
@@ -401,6 +402,10 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
         seq_end = __ldg(&p.seq_offsets[s + 1]);
     }
     int cached_seq = -1;
+    // Spread ranking: each entry's key goes to shared memory as it is scored.
+    uint32_t* spread_key = reinterpret_cast<uint32_t*>(smem_dec + p.frag_bytes_cta);
+    const int64_t spread_first =
+        static_cast<int64_t>(blockIdx.x) * p.entries_per_warp * (blockDim.x >> 5);
     int64_t seq_begin = MASKED ? __ldg(&p.seq_offsets[s]) : 0;
     int64_t clen = INT64_MAX, pos0 = INT64_MAX / 2;
     if (MASKED) {
@@ -440,6 +445,7 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
             if (id < 0 || id >= p.max_blocks) {
                 if (lane == 0) {
                     p.scores[i] = INFINITY;
+                    if (p.spread) spread_key[i - spread_first] = rankdev::rank_key<false>(INFINITY);
                     raise_error(p.dev_status, p.lib_error, HSS_ERR_OUT_OF_RANGE);
                 }
                 continue;
@@ -573,7 +579,10 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1)
                 best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, off));
-            if (lane == 0) p.scores[i] = best;
+            if (lane == 0) {
+                p.scores[i] = best;
+                if (p.spread) spread_key[i - spread_first] = rankdev::rank_key<false>(best);
+            }
         }
     }
     }  // has_work
@@ -583,50 +592,80 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
         // ---- spread ranking of the one sequence [a, b): the rank of entry e is the number
         // of words (key << 32 | position) below its own; entry e is victim number rank(e)
         // when that is below k.  The words are unique, so the ranks are a permutation.
+        // Every CTA publishes its entries' keys in the workspace as 64-bit words tagged with
+        // this call's number (tag << 32 | key, one relaxed store each) and reads the
+        // sequence's words until every one carries the tag: each word is its own
+        // completion flag, so no counter, fence or second read of the scores is needed.
         uint32_t* ekey = reinterpret_cast<uint32_t*>(smem_dec + p.frag_bytes_cta);
-        uint32_t* part = ekey + p.todo_cap;  // [warp][kSpreadMaxCta] partial counts
+        uint32_t* part = ekey + p.todo_cap;  // [warp][kSpreadMaxCta] partial counts, then
+        uint32_t* tag_smem = part + kWarpsMax * kSpreadMaxCta;  // this call's tag
         const int64_t per_cta = p.entries_per_warp * (blockDim.x >> 5);
         const int64_t cb = static_cast<int64_t>(blockIdx.x) * per_cta;
         // (loaded before the barrier: the latency overlaps the CTA's slowest warp)
         const int64_t a = __ldg(&p.seq_offsets[0]), b = __ldg(&p.seq_offsets[1]);
         const int64_t eb = max(cb, a), ee = min(min(p.total, cb + per_cta), b);
         const int cnt = ee > eb ? static_cast<int>(ee - eb) : 0;  // <= kSpreadMaxCta
-        const int n = static_cast<int>(min(b, p.total) - a);  // entries the counts reach
-        // Arrive: the barrier orders every warp's scores before thread 0's count, a release
-        // at GPU scope (no reply is awaited).  The additions form one release sequence, so
-        // the acquire load that sees the count complete sees every other CTA's scores.
-        int* arrive = p.counters + kSpreadRegionWords;
-        int* depart = arrive + 32;
-        __syncthreads();
-        if (threadIdx.x == 0 && cnt > 0) {
-            red_add_release_gpu(arrive, cnt);
-            const uint64_t t0 = global_timer_ns();
-            while (ld_acquire_gpu(arrive) < n) {
-                if (global_timer_ns() - t0 > kWaitLimitNs) {
-                    raise_error(p.dev_status, p.lib_error, HSS_ERR_DEVICE_TIMEOUT);
-                    break;
-                }
-            }
+        if (a < 0 || b < a || min(b, p.total) - a > kSpreadMaxEntries) {
+            // Offsets that do not describe one sequence of at most 4096 of the scored
+            // entries: nothing is published (the keys region holds 4096 words).
+            if (threadIdx.x == 0) raise_error(p.dev_status, p.lib_error, HSS_ERR_OUT_OF_RANGE);
+            grid_launch_dependents();
+            return;
         }
-        __syncthreads();
-        grid_launch_dependents();
-        // Words of the sequence (16 per thread; past the end a word above every real one:
-        // NaN and +inf map to key 0xFF800000) and this CTA's own entries' keys.
+        const int n = static_cast<int>(min(b, p.total) - a);
+        int* epoch = p.counters + kSpreadRegionWords;
+        uint64_t* words = reinterpret_cast<uint64_t*>(p.counters + kSpreadWordsOffsetWords);
+        if (threadIdx.x == 0) *tag_smem = static_cast<uint32_t>(ld_relaxed_gpu(epoch)) + 1u;
+        __syncthreads();  // this CTA's keys and the tag
+        if (cnt == 0) {  // no entry of the sequence in this CTA
+            if (blockIdx.x == 0)
+                for (int j = max(n, 0) + static_cast<int>(threadIdx.x); j < p.k; j += blockDim.x)
+                    p.victims[j] = -1;
+            grid_launch_dependents();
+            return;
+        }
+        const uint32_t tag = *tag_smem;
+        const int pos0 = static_cast<int>(eb - a);  // position of this CTA's first entry
+        if (static_cast<int>(threadIdx.x) < cnt)
+            st_relaxed_gpu_u64(&words[pos0 + threadIdx.x],
+                               (static_cast<uint64_t>(tag) << 32) | ekey[eb - cb + threadIdx.x]);
+        // Gather: 16 words per thread (slot q holds position tid + 256 q); slots past the
+        // end hold a word above every real one (NaN and +inf map to key 0xFF800000).
         uint64_t w[kSpreadKeysPerThread];
+        uint32_t missing = 0;
 #pragma unroll
         for (int q = 0; q < kSpreadKeysPerThread; ++q) {
             const int j = static_cast<int>(threadIdx.x) + q * kWarpsMax * 32;
-            w[q] = j < n ? (static_cast<uint64_t>(
-                                rankdev::rank_key<false>(__ldcg(&p.scores[a + j])))
-                            << 32) | static_cast<uint32_t>(j)
-                         : ~0ull;
+            w[q] = ~0ull;
+            if (j < n) missing |= 1u << q;
         }
-        if (static_cast<int>(threadIdx.x) < cnt)
-            ekey[threadIdx.x] = rankdev::rank_key<false>(__ldcg(&p.scores[eb + threadIdx.x]));
-        __syncthreads();
-        // Depart: this CTA reads no counter and no other CTA's score from here on.
-        if (threadIdx.x == 0 && cnt > 0) red_add_relaxed_gpu(depart, 1);
-        const int pos0 = static_cast<int>(eb - a);  // position of this CTA's first entry
+        const uint64_t t0 = global_timer_ns();
+        while (missing != 0) {
+            uint64_t v[kSpreadKeysPerThread];
+#pragma unroll
+            for (int q = 0; q < kSpreadKeysPerThread; ++q) {
+                const int j = static_cast<int>(threadIdx.x) + q * kWarpsMax * 32;
+                v[q] = (missing >> q) & 1u ? ld_relaxed_gpu_u64(&words[j]) : 0ull;
+            }
+#pragma unroll
+            for (int q = 0; q < kSpreadKeysPerThread; ++q) {
+                const int j = static_cast<int>(threadIdx.x) + q * kWarpsMax * 32;
+                if (((missing >> q) & 1u) && static_cast<uint32_t>(v[q] >> 32) == tag) {
+                    w[q] = (v[q] << 32) | static_cast<uint32_t>(j);
+                    missing &= ~(1u << q);
+                }
+            }
+            if (missing != 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+                raise_error(p.dev_status, p.lib_error, HSS_ERR_DEVICE_TIMEOUT);
+                break;
+            }
+        }
+        __syncthreads();  // every thread of this CTA has seen every word
+        grid_launch_dependents();
+        // Every CTA has published, so every CTA has read the tag: the sequence's first CTA
+        // advances the call number for the next call.
+        if (threadIdx.x == 0 && static_cast<int64_t>(blockIdx.x) == a / per_cta)
+            st_relaxed_gpu_s32(epoch, static_cast<int>(tag));
         // Four entries at a time; each warp leaves its four totals in `part`, lane u writing
         // entry e0 + u (no atomics, no branch per entry).  Slots past the sequence hold a word
         // above every real one, so half the slots are skipped whole when n <= 2048.
@@ -636,7 +675,7 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
             uint32_t neg[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                we[u] = e0 + u < cnt ? (static_cast<uint64_t>(ekey[e0 + u]) << 32) |
+                we[u] = e0 + u < cnt ? (static_cast<uint64_t>(ekey[eb - cb + e0 + u]) << 32) |
                                            static_cast<uint32_t>(pos0 + e0 + u)
                                      : 0ull;
                 neg[u] = 0;
@@ -663,21 +702,6 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
         if (blockIdx.x == 0)
             for (int j = n + static_cast<int>(threadIdx.x); j < p.k; j += blockDim.x)
                 p.victims[j] = -1;
-        // The sequence's first CTA clears the counters for the next call once every CTA that
-        // arrived has departed (none of them reads a counter again).
-        if (threadIdx.x == 0 && n > 0 && static_cast<int64_t>(blockIdx.x) == a / per_cta) {
-            const int64_t last_entry = min(p.total, b) - 1;
-            const int ctas = static_cast<int>(last_entry / per_cta - a / per_cta) + 1;
-            const uint64_t t0 = global_timer_ns();
-            while (ld_relaxed_gpu(depart) < ctas) {
-                if (global_timer_ns() - t0 > kWaitLimitNs) {
-                    raise_error(p.dev_status, p.lib_error, HSS_ERR_DEVICE_TIMEOUT);
-                    break;
-                }
-            }
-            *arrive = 0;
-            *depart = 0;
-        }
         return;
     }
 
@@ -883,10 +907,11 @@ hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream, const Fu
     p.spread = 0;
     if (fr != nullptr && fr->counters != nullptr && warps_per_cta == kWarpsMax &&
         a.num_seqs == 1 && a.total <= kSpreadMaxEntries &&
+        (reinterpret_cast<uintptr_t>(fr->counters) & 7u) == 0 &&
         p.entries_per_warp * warps_per_cta <= kSpreadMaxCta) {
         // Spread ranking needs the whole grid resident at once (its CTAs wait for each other).
         const int todo_cap = static_cast<int>(p.entries_per_warp * warps_per_cta);
-        const int smem_spread = smem + 4 * todo_cap + 4 * kWarpsMax * kSpreadMaxCta;
+        const int smem_spread = smem + 4 * todo_cap + 4 * kWarpsMax * kSpreadMaxCta + 16;
         int per_sm = 0;
 #define HSS_DECODE_CASE(KS, NT_) \
     if (ksteps == KS && nt == NT_) per_sm = ctas_per_sm_t<KS, NT_>(p, smem_spread);
