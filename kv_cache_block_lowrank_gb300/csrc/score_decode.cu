@@ -87,8 +87,9 @@ struct DecodeParams {
     // takes the grid dependency wait; num_new <= 32 then.
     int32_t nowait;
     // spread != 0 (one sequence of at most kSpreadMaxEntries entries, every CTA of the grid
-    // resident at once): instead of the last CTA ranking the whole sequence, every CTA waits
-    // until the sequence's count is complete and places its own entries by counting the
+    // resident at once, 8-byte aligned workspace): instead of the last CTA ranking the whole
+    // sequence, every CTA publishes its entries' keys as call-tagged words, waits until every
+    // word of the sequence carries this call's tag and places its own entries by counting the
     // smaller words, so the ranking is spread over the grid.
     int32_t spread;
 };
@@ -273,7 +274,7 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
     const bool nowait = INLINE && p.nowait != 0;
     if (!nowait) grid_dependency_wait();
     // Spread ranking waits for every CTA of this grid: the next kernel may not take their
-    // places (it is let in once all of them have arrived).
+    // places (it is let in once a CTA has seen every CTA's keys).
     if (!p.spread) grid_launch_dependents();
     // nowait: this lane's new id (lane < num_new <= 32); a warp waits before its first one.
     const int32_t my_new = nowait && lane < p.num_new ? __ldg(&p.new_ids[lane]) : -1;
