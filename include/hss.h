@@ -299,8 +299,10 @@ hss_status hss_select_rows(const float* scores, int32_t rows, int64_t num_blocks
  *   scores, victims          outputs, as in hss_score_blocks / hss_rank_victims
  *   workspace                device, >= hss_layer_step_workspace_bytes(num_seqs) bytes,
  *                            4-byte aligned (8-byte aligned for the one-sequence ranking
- *                            above): per-sequence completion counters, then a call number
- *                            and 32 KiB of tagged keys for one sequence.  Zero all of it once
+ *                            above): the one-sequence ranking's call number and 32 KiB of
+ *                            tagged keys (33024 bytes), then the per-sequence completion
+ *                            counters, so calls with different num_seqs may share one
+ *                            workspace sized for the largest.  Zero all of it once
  *                            (e.g. cudaMemsetAsync) before its first use, then leave it as
  *                            each call leaves it: the counters return to zero, the call
  *                            number and the keys carry over to the next call (zeroing all

@@ -246,11 +246,11 @@ hss_status hss_rank_victims(const float* scores, const int32_t* seq_offsets, int
 
 size_t hss_layer_step_workspace_bytes(int32_t num_seqs) {
     if (num_seqs <= 0) return 0;
-    // Per-sequence completion counters (rounded up to 256 bytes), then the one-sequence spread
-    // ranking's call number (256 bytes) and its tagged words (8 bytes for each of at most
-    // 4096 entries).
+    // The one-sequence spread ranking's region (its call number in 256 bytes, then 8 bytes for
+    // each of at most 4096 entries), then the per-sequence completion counters (rounded up to
+    // 256 bytes).
     const size_t b = static_cast<size_t>(num_seqs) * sizeof(int32_t);
-    return (b + 255) / 256 * 256 + 256 + 8 * 4096;
+    return static_cast<size_t>(kSpreadRegionBytes) + (b + 255) / 256 * 256;
 }
 
 hss_status hss_layer_step(const hss_dims* dims, const uint16_t* P, const uint16_t* K_new,
@@ -350,7 +350,8 @@ hss_status hss_layer_step(const hss_dims* dims, const uint16_t* P, const uint16_
             // are projected in the scorer and there are no new blocks: then nothing of this
             // call precedes it and it may read nothing before its dependency wait.
             const bool own_projection = !inline_q || num_new > 0;
-            FusedRank fr{static_cast<int32_t*>(workspace), victims, k, own_projection, new_ids,
+            int32_t* ws = static_cast<int32_t*>(workspace);
+            FusedRank fr{ws + kSpreadRegionBytes / 4, ws, victims, k, own_projection, new_ids,
                          num_new};
             // With the queries projected in the scorer, that projection writes only the new
             // slots, so the scorer need not wait for it anywhere else.

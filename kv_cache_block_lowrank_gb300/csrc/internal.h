@@ -97,8 +97,15 @@ struct ScoreArgs {
 };
 // Victim ranking fused into the decode scorer: counters are the caller's per-sequence
 // completion counters (zero on entry, left zero on exit).
+// The layer-step workspace: first the one-sequence spread ranking's region (a call number in
+// a 256-byte line of its own, then one 8-byte tagged key per entry, at most 4096), then the
+// per-sequence completion counters.  The region comes first so that calls with different
+// numbers of sequences find their counters and it at the same places.
+constexpr int64_t kSpreadRegionBytes = 256 + 8 * 4096;
+
 struct FusedRank {
     int32_t* counters;  // nullptr: no fused ranking
+    int32_t* spread_region;  // the workspace's spread-ranking region (nullptr: none)
     int32_t* victims;
     int32_t k;
     // The kernel launched just before the scorer on this stream writes only Qp and the A_g

@@ -99,10 +99,9 @@ constexpr int kSpreadKeysPerThread = 16;
 constexpr int kSpreadMaxEntries = kWarpsMax * 32 * kSpreadKeysPerThread;
 // ... and the most entries one CTA scores and places (2 per warp at 4096 entries on 152 SMs).
 constexpr int kSpreadMaxCta = 16;
-// Its workspace region follows the one sequence's counter (256 bytes in): the call number (a
-// line of its own), then from byte 512 one tagged word per entry (32 KiB).
-constexpr int kSpreadRegionWords = 64;
-constexpr int kSpreadWordsOffsetWords = 128;
+// Its workspace region (p.counters in spread mode): the call number (a line of its own), then
+// from byte 256 one tagged word per entry (32 KiB).
+constexpr int kSpreadWordsOffsetWords = 64;
 
 // below -= [w < we] for 64-bit unsigned words: one borrow chain, no predicate or branch (a
 // compare-and-select per pair issued about twice the instructions).
@@ -614,7 +613,7 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
             return;
         }
         const int n = static_cast<int>(min(b, p.total) - a);
-        int* epoch = p.counters + kSpreadRegionWords;
+        int* epoch = p.counters;
         uint64_t* words = reinterpret_cast<uint64_t*>(p.counters + kSpreadWordsOffsetWords);
         if (threadIdx.x == 0) *tag_smem = static_cast<uint32_t>(ld_relaxed_gpu(epoch)) + 1u;
         __syncthreads();  // this CTA's keys and the tag
@@ -906,9 +905,9 @@ hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream, const Fu
     const int ksteps = a.r / 16;
     const int nt = (p.nvec + 7) / 8;
     p.spread = 0;
-    if (fr != nullptr && fr->counters != nullptr && warps_per_cta == kWarpsMax &&
+    if (fr != nullptr && fr->spread_region != nullptr && warps_per_cta == kWarpsMax &&
         a.num_seqs == 1 && a.total <= kSpreadMaxEntries &&
-        (reinterpret_cast<uintptr_t>(fr->counters) & 7u) == 0 &&
+        (reinterpret_cast<uintptr_t>(fr->spread_region) & 7u) == 0 &&
         p.entries_per_warp * warps_per_cta <= kSpreadMaxCta) {
         // Spread ranking needs the whole grid resident at once (its CTAs wait for each other).
         const int todo_cap = static_cast<int>(p.entries_per_warp * warps_per_cta);
@@ -928,7 +927,7 @@ hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream, const Fu
         if (static_cast<int64_t>(per_sm) * dev->num_sms >= grid) {
             p.spread = 1;
             p.todo_cap = todo_cap;
-            p.counters = fr->counters;
+            p.counters = fr->spread_region;  // the tail's call number and tagged words
             p.victims = fr->victims;
             p.k = fr->k;
             smem = smem_spread;

@@ -167,8 +167,8 @@ def _load_fresh(mod, path):
 
 def test_layer_step_validation(lib):
     assert hss.hss_layer_step_workspace_bytes(0) == 0
-    assert hss.hss_layer_step_workspace_bytes(1) == 256 + 256 + 32768
-    assert hss.hss_layer_step_workspace_bytes(65) == 512 + 256 + 32768
+    assert hss.hss_layer_step_workspace_bytes(1) == 33024 + 256
+    assert hss.hss_layer_step_workspace_bytes(65) == 33024 + 512
     base = lambda **o: [o.get("d", dims()), FAKE, FAKE, FAKE, o.get("num_new", 1), FAKE, 1, FAKE,
                         FAKE, o.get("layer", 0), FAKE, FAKE, o.get("S", 1), 10, FAKE,
                         o.get("k", 4), FAKE, o.get("ws", FAKE), o.get("wsb", 65536), None, 0]

@@ -20,12 +20,15 @@ def built():
     hss.load()
 
 
+SPREAD_REGION_WORDS = 33024 // 4  # the one-sequence ranking's call number and tagged keys
+
+
 def counters_zero(ws, num_seqs):
-    """The per-sequence completion counters (the workspace's first 4 * num_seqs bytes, rounded
-    up to 256) are back at zero; the one-sequence ranking's call number and keys after them
-    carry over to the next call."""
+    """The per-sequence completion counters (4 * num_seqs bytes, rounded up to 256, after the
+    one-sequence ranking's region) are back at zero; that region carries over to the next
+    call."""
     words = (4 * num_seqs + 255) // 256 * 64
-    return int(ws[:words].abs().sum()) == 0
+    return int(ws[SPREAD_REGION_WORDS:SPREAD_REGION_WORDS + words].abs().sum()) == 0
 
 
 def make(dims, lengths, rows, n_new, seed, pool_extra=7):
@@ -269,3 +272,18 @@ def test_layer_step_one_sequence_bad_id():
     assert int(vic[0, -1]) == 777
     assert counters_zero(ws, 1)
     assert hss.hss_read_device_error() == hss.HSS_ERR_OUT_OF_RANGE
+
+
+def test_layer_step_one_workspace_for_every_sequence_count():
+    # One workspace sized for the largest batch serves calls with one sequence (spread
+    # ranking: call number and tagged keys) and with many (per-sequence counters, the last
+    # CTA ranks), in any order.
+    d = W.Dims(1, 32, 8, 128, 32, 16, 3000)
+    ws = torch.zeros(hss.hss_layer_step_workspace_bytes(80) // 4, dtype=torch.int32, device=DEV)
+    for i, lengths in enumerate(([2048], [30] * 80, [1500], [10] * 70 + [5], [700], [2048])):
+        x = make(d, lengths, 1, 1, seed=100 + i)
+        _, _, sc1, vic1 = separate(d, x, 0, 16)
+        _, _, sc2, vic2, _ = fused(d, x, 0, 16, ws=ws)
+        assert torch.equal(sc1, sc2)
+        assert torch.equal(vic1, vic2), f"call {i}: {len(lengths)} sequences"
+        assert counters_zero(ws, 80)
