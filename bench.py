@@ -259,6 +259,13 @@ class DecodeWorkload(_Base):
         self.ws_bytes = hss.hss_layer_step_workspace_bytes(1)
         self.hdims = hss.hss_dims.of(d)
         self.ws = torch.zeros(self.ws_bytes // 4, dtype=torch.int32, device=device)
+        # The layer call with its fixed arguments bound once (Qp = NULL: the caller wants
+        # scores and victims, not the projected queries, so the decode scorer projects them).
+        self.step_call = hss.LayerStep(self.hdims, self.P, self.new_ids, 1, 1, None, self.A,
+                                       self.table, self.offs, 1, self.n, self.k, self.ws,
+                                       self.ws_bytes)
+        self.score_ptrs = [self.scores[l].data_ptr() for l in range(self.L)]
+        self.victim_ptrs = [self.victims[l].data_ptr() for l in range(self.L)]
         torch.cuda.synchronize()
 
     units_per_step = property(lambda self: self.L * self.n)
@@ -269,11 +276,7 @@ class DecodeWorkload(_Base):
         K_new = self.K_new[l] if K_new is None else K_new
         Q = self.Q[l] if Q is None else Q
         if not self.unfused:
-            # Qp = NULL: the caller wants scores and victims, not the projected queries, so the
-            # decode scorer projects them itself.  The dims go in as the prebuilt C struct.
-            hss.hss_layer_step(self.hdims, self.P, K_new, self.new_ids, 1, Q, 1, None, self.A, l,
-                               self.table, self.offs, 1, self.n, self.scores[l], self.k,
-                               self.victims[l], self.ws, self.ws_bytes, stream=stream)
+            self.step_call(l, K_new, Q, self.score_ptrs[l], self.victim_ptrs[l], stream=stream)
             return
         hss.hss_project_kv_blocks(d, self.P, K_new, l, self.new_ids, 1, self.A)
         hss.hss_project_q(d, self.P, Q, 1, self.Qp[l])
@@ -326,13 +329,15 @@ class DecodeWorkload(_Base):
                     for l in range(self.L)]
         self.d_K = [self.d_in[self.L * q_el + l * k_el:self.L * q_el + (l + 1) * k_el]
                     .view(self.K_new[0].shape) for l in range(self.L)]
+        self.d_Q_ptrs = [t.data_ptr() for t in self.d_Q]
+        self.d_K_ptrs = [t.data_ptr() for t in self.d_K]
         self.h_vic = torch.empty(self.L, 1, self.k, dtype=torch.int32).pin_memory()
 
     def e2e_step(self):
         self.d_in.copy_(self.h_in, non_blocking=True)
         stream = self.torch.cuda.current_stream().cuda_stream  # one lookup per step
         for l in range(self.L):
-            self.layer_call(l, K_new=self.d_K[l], Q=self.d_Q[l], stream=stream)
+            self.layer_call(l, K_new=self.d_K_ptrs[l], Q=self.d_Q_ptrs[l], stream=stream)
         self.h_vic.copy_(self.victims, non_blocking=True)
         self.torch.cuda.current_stream().synchronize()
 

@@ -274,6 +274,37 @@ def hss_layer_step(dims, P, K_new, new_ids, num_new: int, Q, rows_per_seq: int, 
     _check(st, "hss_layer_step")
 
 
+class LayerStep:
+    """hss_layer_step with the arguments that stay the same from call to call bound once.
+
+    A serving loop makes one layer call per layer and step with the same dims, P, A_g,
+    block table, offsets, workspace and sizes; binding them here leaves only the per-call
+    ones (layer, the new key blocks, the queries, the score and victim buffers, the stream)
+    to marshal.  Tensors or integer device addresses are accepted for those; the call is
+    exactly hss_layer_step (same C entry point, same arguments).
+    """
+
+    def __init__(self, dims, P, new_ids, num_new: int, rows_per_seq: int, Qp, A_g,
+                 block_table, seq_offsets, num_seqs: int, total_blocks: int, k: int,
+                 workspace, workspace_bytes: int, dev_status=None):
+        vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        self._fn = load().hss_layer_step
+        self._dims = hss_dims.of(dims)  # kept alive: the call passes its address
+        self._head = (ctypes.byref(self._dims), vp(_ptr(P)))
+        self._mid1 = (vp(_ptr(new_ids)), i64(int(num_new)))
+        self._mid2 = (i32(int(rows_per_seq)), vp(_ptr(Qp)), vp(_ptr(A_g)))
+        self._mid3 = (vp(_ptr(block_table)), vp(_ptr(seq_offsets)), i32(int(num_seqs)),
+                      i64(int(total_blocks)))
+        self._k = i32(int(k))
+        self._tail = (vp(_ptr(workspace)), sz(int(workspace_bytes)), vp(_ptr(dev_status)))
+
+    def __call__(self, layer: int, K_new, Q, scores, victims, stream=None) -> None:
+        st = self._fn(*self._head, _ptr(K_new), *self._mid1, _ptr(Q), *self._mid2, int(layer),
+                      *self._mid3, _ptr(scores), self._k, _ptr(victims), *self._tail,
+                      _stream(stream))
+        _check(st, "hss_layer_step")
+
+
 def hss_layer_step_static_max_seqs() -> int:
     return load().hss_layer_step_static_max_seqs()
 

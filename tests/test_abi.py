@@ -191,3 +191,21 @@ def test_self_test_validation(lib):
     assert status_of(hss.hss_self_test_wait_timeout, FAKE, 10, 0) == hss.HSS_ERR_INVALID_ARGUMENT
     assert status_of(hss.hss_self_test_wait_timeout, FAKE, 3 * 10 ** 9, 0) == \
         hss.HSS_ERR_INVALID_ARGUMENT
+
+
+def test_layer_step_prepared_call_marshals_like_the_plain_call(lib):
+    # The bound-arguments form reaches the same C entry point with the same arguments: each
+    # validation error of the plain call comes back from it too (argument positions included).
+    def both(layer=0, k=4, wsb=65536, num_new=1, ws=FAKE):
+        plain = status_of(hss.hss_layer_step, dims(), FAKE, FAKE, FAKE, num_new, FAKE, 1, FAKE,
+                          FAKE, layer, FAKE, FAKE, 1, 10, FAKE, k, FAKE, ws, wsb, None, 0)
+        step = hss.LayerStep(dims(), FAKE, FAKE, num_new, 1, FAKE, FAKE, FAKE, FAKE, 1, 10, k,
+                             ws, wsb)
+        return plain, status_of(step, layer, FAKE, FAKE, FAKE, FAKE, 0)
+
+    for kw, want in [({"layer": 99}, hss.HSS_ERR_OUT_OF_RANGE),
+                     ({"k": 0}, hss.HSS_ERR_INVALID_ARGUMENT),
+                     ({"num_new": -1}, hss.HSS_ERR_INVALID_ARGUMENT),
+                     ({"wsb": 16}, hss.HSS_ERR_WORKSPACE_TOO_SMALL),
+                     ({"ws": None}, hss.HSS_ERR_NULL_POINTER)]:
+        assert both(**kw) == (want, want), kw

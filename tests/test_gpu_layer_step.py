@@ -287,3 +287,35 @@ def test_layer_step_one_workspace_for_every_sequence_count():
         assert torch.equal(sc1, sc2)
         assert torch.equal(vic1, vic2), f"call {i}: {len(lengths)} sequences"
         assert counters_zero(ws, 80)
+
+
+@pytest.mark.parametrize("inline", [True, False])
+def test_prepared_layer_step_equals_the_plain_call(inline):
+    # hss.LayerStep binds the arguments that stay fixed across calls; each call must give
+    # exactly what hss_layer_step gives (the decode layer, 32 layers of one step).
+    d = W.Dims(4, 32, 8, 128, 32, 16, 2100)
+    x = make(d, [2048], 1, 1, seed=11)
+    k = 256
+    nb = hss.hss_layer_step_workspace_bytes(1)
+    Qp = None if inline else torch.empty(1, 1, d.num_q_heads, d.r, dtype=torch.bfloat16,
+                                         device=DEV)
+    out = []
+    for prepared in (False, True):
+        A = x["A"].clone()
+        ws = torch.zeros(nb // 4, dtype=torch.int32, device=DEV)
+        sc = torch.empty(d.num_layers, 2048, dtype=torch.float32, device=DEV)
+        vic = torch.full((d.num_layers, 1, k), 12345, dtype=torch.int32, device=DEV)
+        step = hss.LayerStep(d, x["P"], x["new_ids"], 1, 1, Qp, A, x["table"], x["offs"], 1,
+                             2048, k, ws, nb)
+        for layer in range(d.num_layers):
+            if prepared:
+                step(layer, x["K_new"], x["Q"], sc[layer].data_ptr(), vic[layer])
+            else:
+                hss.hss_layer_step(d, x["P"], x["K_new"], x["new_ids"], 1, x["Q"], 1, Qp, A,
+                                   layer, x["table"], x["offs"], 1, 2048, sc[layer], k,
+                                   vic[layer], ws, nb)
+        torch.cuda.synchronize()
+        out.append((A, sc, vic))
+    assert torch.equal(out[0][0].view(torch.int16), out[1][0].view(torch.int16))
+    assert torch.equal(out[0][1], out[1][1])
+    assert torch.equal(out[0][2], out[1][2])
