@@ -67,3 +67,30 @@ def test_defaults_and_peaks():
     assert a.gpus == 1 and a.warmup >= 3 and a.steps > 0 and a.impl == "hss"
     p = bench.measured_peaks()
     assert p["hbm_gbs"] > 1000 and p["bf16_tflops"] > 100
+
+
+def test_reference_arm_prints_one_contract_line():
+    # `bench.py --impl reference` times the oracle (the CPU restatement of the method) on the
+    # host; its single JSON line carries the contract's keys with the decode workload's
+    # metric, and an e2e entry that moves no bytes between host and device.
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                          "--warmup", "3"], cwd=root, capture_output=True, text=True,
+                         timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config"):
+        assert key in d, key
+    assert d["value"] > 0 and d["unit"] == "blocks/s" and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
