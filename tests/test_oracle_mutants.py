@@ -87,6 +87,14 @@ MUTANTS = [
     ("select_nan_first", "v = isnan(v) ? INFINITY : -v;", "v = isnan(v) ? -INFINITY : -v;", 0),
     ("token_status_counts_padding", "if (slots[i] >= max_blocks * block_size) {",
      "if (slots[i] < 0 || slots[i] >= max_blocks * block_size) {", 0),
+    ("victims_global_index", "keyed[i].idx = (int32_t)i;\n        }\n        qsort(keyed, (size_t)n,",
+     "keyed[i].idx = (int32_t)(base + i);\n        }\n        qsort(keyed, (size_t)n,", 0),
+    ("select_no_minus_one_pad", "lists[r * (int64_t)topk + i] = i < complete ? keyed[i].idx : -1;",
+     "lists[r * (int64_t)topk + i] = i < complete ? keyed[i].idx : 0;", 0),
+    ("select_ignores_first_pos", "int64_t complete = (first_pos + r + 1) / block_size;",
+     "int64_t complete = (r + 1) / block_size;", 0),
+    ("select_row_stride_is_n", "double v = (double)scores[r * stride + j];",
+     "double v = (double)scores[r * n + j];", 0),
 ]
 
 
