@@ -95,6 +95,16 @@ MUTANTS = [
      "int64_t complete = (r + 1) / block_size;", 0),
     ("select_row_stride_is_n", "double v = (double)scores[r * stride + j];",
      "double v = (double)scores[r * n + j];", 0),
+    ("score_drops_last_token", "for (int t = 0; t < k->bs; ++t) {\n                const uint16_t* a",
+     "for (int t = 0; t + 1 < k->bs; ++t) {\n                const uint16_t* a", 0),
+    ("score_drops_last_head", "for (int h = 0; h < k->nq; ++h) {", "for (int h = 0; h + 1 < k->nq; ++h) {",
+     0),
+    ("score_drops_last_row", "for (int row = 0; row < k->rows; ++row) {",
+     "for (int row = 0; row + 1 < k->rows; ++row) {", 0),
+    ("tsum_signed", "mag += fabs(term);", "mag += term;", 0),
+    ("masked_max_floor_zero", "double best = -INFINITY;", "double best = 0.0;", 1),
+    ("masked_drops_last_head", "for (int h = 0; h < k->nq; ++h) {", "for (int h = 0; h + 1 < k->nq; ++h) {",
+     1),
 ]
 
 
