@@ -15,7 +15,9 @@ import oracle_pins as pins
 SRC = open(os.path.join(os.path.dirname(oracle.__file__), "hss_oracle.c")).read()
 
 # (name, text to replace, replacement, which occurrence (0-based)).
-# Not listed, because they are equivalent mutants (no input tells them apart):
+# Not listed: the sign of a NaN's bf16 pattern (IEEE 754 leaves a NaN's sign unspecified
+# for conversions and PyTorch itself gives 0xFFFF for both signs, so nothing outside the
+# oracle fixes it), and, because they are equivalent mutants (no input tells them apart):
 # loosening the explicit overflow test in the bf16 rounding (the binary32
 # conversion of 2^128 is +inf anyway), and dropping the -0 -> +0 step of the
 # per-row selection (its comparator already orders -0 and +0 as equal).
@@ -105,6 +107,8 @@ MUTANTS = [
     ("masked_max_floor_zero", "double best = -INFINITY;", "double best = 0.0;", 1),
     ("masked_drops_last_head", "for (int h = 0; h < k->nq; ++h) {", "for (int h = 0; h + 1 < k->nq; ++h) {",
      1),
+    ("overflow_saturates", "y = copysign(INFINITY, x);", "y = copysign(0x1.FEp127, x);", 0),
+    ("bf16_widen_wrong_shift", "uint32_t u = ((uint32_t)b) << 16;", "uint32_t u = ((uint32_t)b) << 15;", 0),
 ]
 
 
