@@ -109,6 +109,9 @@ MUTANTS = [
      1),
     ("overflow_saturates", "y = copysign(INFINITY, x);", "y = copysign(0x1.FEp127, x);", 0),
     ("bf16_widen_wrong_shift", "uint32_t u = ((uint32_t)b) << 16;", "uint32_t u = ((uint32_t)b) << 15;", 0),
+    ("kv_bad_position_zero_based", "            return i + 1;", "            return i;", 0),
+    ("token_cache_not_written", "memcpy(crow, krow, (size_t)k->hd * sizeof(uint16_t));",
+     "(void)crow;", 0),
 ]
 
 
