@@ -106,6 +106,51 @@ def pin_bf16_matches_torch(L):
     assert np.array_equal(back, from_bf16_bits(exp))
 
 
+def pin_projection_single_rounding(L):
+    """Every projection sums in more precision than binary32 and rounds once, to bf16.
+
+    Hand case: a key/query row [1, 2^-8, 2^-30, 0, ...] against P columns of +-1 on the
+    first three coordinates.  The exact sum 1 + 2^-8 + 2^-30 lies just above the midpoint
+    between the bf16 neighbours 1 (0x3F80) and 1 + 2^-7 (0x3F81), so it rounds up to 0x3F81
+    (and its negative to 0xBF81).  A binary32 running sum drops the 2^-30 term (it is below
+    half a binary32 step at 1) and lands on the midpoint itself, which ties to even: 0x3F80.
+    Rounding the exact sum to binary32 first does the same.  The row 1 + 2^-8 - 2^-30 lies
+    just below the midpoint (0x3F80 either way), and 2^-30 alone is 0x3080.
+    Checked through all three projections: queries, key blocks and key tokens.
+    """
+    hd, r, bs = 16, 4, 2
+    row = np.zeros(hd)
+    row[:3] = [1.0, 2.0 ** -8, 2.0 ** -30]
+    Pf = np.zeros((hd, r))
+    Pf[:3, 0] = 1.0
+    Pf[:3, 1] = -1.0
+    Pf[:3, 2] = [1.0, 1.0, -1.0]
+    Pf[2, 3] = 1.0
+    P = to_bf16_bits(Pf)
+    # The row's entries are powers of two: exact in bf16.
+    assert np.array_equal(from_bf16_bits(to_bf16_bits(row)), row)
+    exp = np.array([0x3F81, 0xBF81, 0x3F80, 0x3080], dtype=np.uint16)
+    rev = row.copy()
+    rev[:3] = row[2::-1]                       # the same terms in reverse order
+    Prev = to_bf16_bits(Pf[[2, 1, 0] + list(range(3, hd))])
+    Q = to_bf16_bits(np.stack([row, row]))
+    qp = oracle.project_q(Q, P, L=L)
+    assert np.array_equal(qp[0], exp) and np.array_equal(qp[1], exp), qp
+    qp_rev = oracle.project_q(to_bf16_bits(rev[None]), Prev, L=L)
+    assert np.array_equal(qp_rev[0], exp), qp_rev
+    # Key block: both tokens of the one kv head carry the row (second one negated).
+    K = to_bf16_bits(np.stack([row, -row])[None, :, None, :])      # [1, bs, 1, hd]
+    A = np.zeros((1, 1, 1, bs, r), dtype=np.uint16)
+    assert oracle.project_kv_blocks(P, K, 0, np.array([0], dtype=np.int32), A, L=L) == 0
+    assert np.array_equal(A[0, 0, 0, 0], exp), A[0, 0, 0, 0]
+    assert np.array_equal(A[0, 0, 0, 1], exp ^ 0x8000), A[0, 0, 0, 1]
+    # Key tokens: the same two rows written one token at a time, in reverse slot order.
+    A_t = np.zeros_like(A)
+    K_tok = to_bf16_bits(np.stack([-row, row])[:, None, :])        # [2, 1, hd]
+    assert oracle.write_kv_tokens(P, K_tok, np.array([1, 0]), 0, A_t, L=L) == 0
+    assert np.array_equal(A_t, A), A_t
+
+
 # ----------------------------------------------------------------------------- method pins
 
 def _grid_case(rng, *, nq, nkv, hd, bs, S, R, lengths, layers, layer, pool):
@@ -564,6 +609,7 @@ def pin_rows_selection_hand_case(L):
 ALL_PINS = [
     pin_bf16_hand_values,
     pin_bf16_matches_torch,
+    pin_projection_single_rounding,
     pin_identity_projection_brute_force,
     pin_selection_projection_brute_force,
     pin_gqa_contiguous_groups,

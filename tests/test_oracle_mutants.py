@@ -112,6 +112,18 @@ MUTANTS = [
     ("kv_bad_position_zero_based", "            return i + 1;", "            return i;", 0),
     ("token_cache_not_written", "memcpy(crow, krow, (size_t)k->hd * sizeof(uint16_t));",
      "(void)crow;", 0),
+    ("q_float_accumulator", "double acc = 0.0;\n        for (int d = 0; d < k->hd; ++d) {\n            acc +=",
+     "float acc = 0.0;\n        for (int d = 0; d < k->hd; ++d) {\n            acc +=", 0),
+    ("kv_float_accumulator", "double acc = 0.0;\n                for (int d = 0; d < k->hd; ++d) {\n                    acc +=",
+     "float acc = 0.0;\n                for (int d = 0; d < k->hd; ++d) {\n                    acc +=", 0),
+    ("token_float_accumulator", "double acc = 0.0;\n            for (int d = 0; d < k->hd; ++d) {\n                acc +=",
+     "float acc = 0.0;\n            for (int d = 0; d < k->hd; ++d) {\n                acc +=", 0),
+    ("q_rounds_through_float", "k->Qp[v * k->r + j] = orc_bf16_from_double(acc);",
+     "k->Qp[v * k->r + j] = orc_bf16_from_double((double)(float)acc);", 0),
+    ("kv_rounds_through_float", "slot[((int64_t)h * k->bs + t) * k->r + j] = orc_bf16_from_double(acc);",
+     "slot[((int64_t)h * k->bs + t) * k->r + j] = orc_bf16_from_double((double)(float)acc);", 0),
+    ("token_rounds_through_float", "arow[j] = orc_bf16_from_double(acc);",
+     "arow[j] = orc_bf16_from_double((double)(float)acc);", 0),
 ]
 
 
