@@ -45,29 +45,37 @@ def abs_sum_scale(X_bits: np.ndarray, P_bits: np.ndarray) -> np.ndarray:
 
 
 def assert_bf16_within_ulp(gpu_bits, orc_bits, max_ulp: int = 1, what: str = "",
-                           scale=None, n_terms: int = 0):
+                           scale=None, n_terms: int = 0, max_cancel_frac: float = 1e-3):
     """bf16 results within max_ulp of the oracle's.
 
     Where `scale` (sum of |terms| of each output) is given, an output may instead lie within
     1 ulp plus the fp32 accumulation bound 2 * n_terms * 2^-24 * scale: when the exact sum
     nearly cancels, one bf16 step of the small result is finer than any fp32 accumulation
-    can resolve, for the GPU and for any other fp32 implementation alike.
+    can resolve, for the GPU and for any other fp32 implementation alike.  `scale` is an
+    array shaped like the outputs, or a function from flat output indices to their scales
+    (evaluated only where an output is more than max_ulp off).  The outputs that need this
+    allowance are counted, and their number is bounded by max(4, max_cancel_frac * size),
+    so that a systematic error cannot hide inside it.
     """
-    g = np.asarray(gpu_bits)
-    o = np.asarray(orc_bits)
+    g = np.asarray(gpu_bits).reshape(-1)
+    o = np.asarray(orc_bits).reshape(-1)
     d = np.abs(ordered(g) - ordered(o))
     bad = d > max_ulp
     n_off = int((d > 0).sum())
     n_cancel = 0
     if scale is not None and bad.any():
+        idx = np.flatnonzero(bad)
+        sc = scale(idx) if callable(scale) else np.asarray(scale).reshape(-1)[idx]
         f = lambda b: (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-        allow = bf16_ulp(o) + 2.0 * n_terms * 2.0 ** -24 * np.asarray(scale)
-        cancel = bad & (np.abs(f(g) - f(o)) <= allow)
+        allow = bf16_ulp(o[idx]) + 2.0 * n_terms * 2.0 ** -24 * np.asarray(sc)
+        cancel = np.abs(f(g[idx]) - f(o[idx])) <= allow
         n_cancel = int(cancel.sum())
-        bad = bad & ~cancel
+        bad[idx[cancel]] = False
     worst = int(d.max()) if d.size else 0
     assert not bad.any(), (f"{what}: {int(bad.sum())} of {d.size} beyond tolerance "
                            f"({n_off} differ at all, worst {worst} ulp)")
+    assert n_cancel <= max(4, max_cancel_frac * d.size), (
+        f"{what}: {n_cancel} of {d.size} outputs needed the cancellation allowance")
     return n_off, n_cancel
 
 
@@ -190,3 +198,24 @@ def slot_scale(case, li: int, block_positions) -> np.ndarray:
 
 def q_scale(case, q_layer: int = 0) -> np.ndarray:
     return abs_sum_scale(bits(case.Q[q_layer]), bits(case.P))
+
+
+def _bf16_f64(b) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(
+        np.float64)
+
+
+def slot_scale_fn(K: torch.Tensor, P: torch.Tensor):
+    """Lazy sum_d |K_d| |P_dj| for A_g slots made from the key blocks K [n, bs, nkv, hd]
+    (any device): a function from flat indices into [n, nkv, bs, r] to their scales."""
+    n, bs, nkv, hd = K.shape
+    Pa = np.abs(_bf16_f64(bits(P)))
+    r = Pa.shape[1]
+
+    def f(idx):
+        blk, h, t, j = np.unravel_index(np.asarray(idx), (n, nkv, bs, r))
+        dev = K.device
+        rows = K[torch.as_tensor(blk, device=dev), torch.as_tensor(t, device=dev),
+                 torch.as_tensor(h, device=dev)]
+        return (np.abs(_bf16_f64(bits(rows))) * Pa[:, j].T).sum(axis=1)
+    return f
