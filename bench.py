@@ -53,6 +53,9 @@ def parse_args(argv=None):
                    help="threads for the oracle's CPU legs (0: every core this process may use)")
     p.add_argument("--layers", type=int, default=32,
                    help="ingest workloads: layers written per step (1: a small case for ncu)")
+    p.add_argument("--no-extras", action="store_true",
+                   help="decode: skip the short passes of the batched, prefill and ingest "
+                        "workloads reported under 'workloads'")
     return p.parse_args(argv)
 
 
@@ -190,7 +193,7 @@ def measured_peaks():
 # dram__bytes_write.sum) from the ncu captures summarised in profiles/, or None when the
 # kernel has changed since its capture.
 TRAFFIC = {
-    "decode": (16853248 + 0, "profiles/score_decode_plain.md"),
+    "decode": None,  # the layer-step kernel changed since its last capture
     "batched": (283580928 + 2741504, "profiles/score_decode_batched.md"),
     "prefill": (140040192 + 3555584, "profiles/score_tc_prefill.md"),
     # captured on a 40000-block launch; traffic grows with the blocks, so scaled to 4096
@@ -269,6 +272,8 @@ class DecodeWorkload(_Base):
         torch.cuda.synchronize()
 
     units_per_step = property(lambda self: self.L * self.n)
+    # hss_layer_step with Qp = NULL: the new block's projection, then the scorer (which
+    # projects the query, scores and ranks), two launches per layer call.
     launches_per_step = property(lambda self: self.L * (4 if self.unfused else 2))
 
     def layer_call(self, l: int, K_new=None, Q=None, stream=None):
@@ -288,16 +293,47 @@ class DecodeWorkload(_Base):
         for l in range(self.L):
             self.layer_call(l)
 
-    # The dominant kernel: the scorer, one launch per layer (32 cold layers per replay).
-    dominant_kernel = "score_decode"
+    # The dominant kernel: the decode scorer as the step runs it, timed per layer call (the
+    # scorer, which projects the query, scores and ranks, after the small kernel projecting
+    # the new block), 32 calls per replay.  Algorithmic bytes of one layer call: every entry's
+    # A_g slot, table id and score; the query, P and the new key block read; the new slot and
+    # the victims written; the sequence offsets.
     dominant_bound = "hbm"
     dominant_launches = property(lambda self: self.L)
-    dominant_units = property(lambda self: self.score_bytes(self.n))
+
+    @property
+    def dominant_kernel(self):
+        return ("score_decode (the plain scorer, hss_score_blocks)" if self.unfused else
+                "score_decode as hss_layer_step runs it, per layer call (the new block's "
+                "projection kernel, then the scorer: query projected, 2048 blocks scored by "
+                "bulk copies into shared memory, bottom-256 ranked)")
+
+    @property
+    def dominant_units(self):
+        if self.unfused:
+            return self.score_bytes(self.n)
+        d = self.dims
+        return (self.n * (self.slot_bytes() + 4 + 4) + d.num_q_heads * d.head_dim * 2 +
+                d.head_dim * d.r * 2 + d.block_size * d.num_kv_heads * d.head_dim * 2 +
+                self.slot_bytes() + self.k * 4 + 8)
 
     def dominant(self):
+        if self.unfused:
+            self.plain_scorer()
+        else:
+            self.step()
+
+    def plain_scorer(self):
         for l in range(self.L):
             self.hss.hss_score_blocks(self.dims, self.Qp[l], 1, self.A, l, self.table, self.offs,
                                       1, self.n, self.scores[l])
+
+    def secondary(self):
+        """The plain scorer (hss_score_blocks on a stored Qp), timed the same way:
+        (name, function, launches per replay, algorithmic bytes per launch)."""
+        for l in range(self.L):
+            self.hss.hss_project_q(self.dims, self.P, self.Q[l], 1, self.Qp[l])
+        return ("plain_scorer", self.plain_scorer, self.L, self.score_bytes(self.n))
 
     def describe(self):
         d = self.dims
@@ -644,6 +680,16 @@ class IngestWorkload(_Base):
             self.hss.hss_project_kv_blocks(self.dims, self.P, self.K[l], l, self.new_ids, nb,
                                            self.A)
 
+    def secondary(self):
+        """The score of the whole step's layer (65536 blocks, one hss_score_blocks launch),
+        timed on its own."""
+        self.hss.hss_project_q(self.dims, self.P, self.Q, 1, self.Qp)
+
+        def score():
+            self.hss.hss_score_blocks(self.dims, self.Qp, 1, self.A, self.layer, self.table,
+                                      self.offs, 1, self.n, self.scores)
+        return ("c5_score", score, 1, self.score_bytes(self.n))
+
     def describe(self):
         return (f"ingest + score under skew: {self.new_ids.numel()} new blocks projected into "
                 f"each of {self.L} layers (K with 4 outlier channels x20 and log-normal token "
@@ -910,6 +956,138 @@ def run_reference(args):
     return 0
 
 
+def time_launches(fn, stream, reps: int, launches: int) -> float:
+    """Seconds per launch: a CUDA graph of `fn` (`launches` back-to-back launches) replayed
+    `reps` times, timed with CUDA events on the launching stream (gaps between graph nodes
+    included)."""
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / (reps * launches)
+
+
+def roofline_of(bound: str, units: float, sec: float, peaks: dict) -> dict:
+    if bound == "hbm":
+        return {"bound": "hbm", "achieved": units / sec / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": units / sec / 1e9 / peaks["hbm_gbs"],
+                "peak_source": peaks["source"] + " hbm_gbs (copy)"}
+    return {"bound": "tensor", "achieved": units / sec / 1e12, "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": units / sec / 1e12 / peaks["bf16_tflops"],
+            "peak_source": peaks["source"] + " bf16_tflops (burst, cuBLAS)"}
+
+
+def run_timed(wl, stream, steps: int, warmup: int, use_graph: bool, world: int, device,
+              min_seconds: float = 0.0):
+    """Warm up, capture the step into a graph, time `steps` steps (rounded to whole replays;
+    with min_seconds > 0, as many more as that many seconds take).  Returns
+    (steps timed, max elapsed over ranks, total units, clock summary)."""
+    import torch
+
+    per_replay = getattr(wl, "graph_steps", 1)
+    capture = getattr(wl, "steps_for_graph", wl.step)
+    with torch.cuda.stream(stream):
+        for _ in range(max(warmup, 3)):
+            capture()
+    stream.synchronize()
+    graph = None
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            capture()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+    run_replay = graph.replay if graph is not None else capture
+    replays = max(1, steps // per_replay)
+    if min_seconds > 0:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(3):
+                run_replay()
+            e1.record(stream)
+        stream.synchronize()
+        per = e0.elapsed_time(e1) / 1e3 / 3
+        replays = max(replays, int(min_seconds / max(per, 1e-9)) + 1)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(world, device)
+    torch.cuda.synchronize()
+    with ClockSampler(device_uuid(torch.cuda.current_device())) as clocks:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(replays):
+                run_replay()
+            ev1.record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize()
+    barrier(world, device)
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    n_steps = replays * per_replay
+    elapsed_max, units = aggregate(elapsed, wl.units_per_step * n_steps, world, device)
+    return n_steps, elapsed_max, units, clocks.summary()
+
+
+def dominant_roofline(wl, stream, peaks, reps: int, traffic=None) -> dict:
+    sec = time_launches(wl.dominant, stream, reps, wl.dominant_launches)
+    r = roofline_of(wl.dominant_bound, wl.dominant_units, sec, peaks)
+    r.update({"kernel": wl.dominant_kernel, "traffic": traffic[0] if traffic else None,
+              "traffic_source": traffic[1] if traffic else "not captured since the kernel "
+                                                               "changed",
+              "launch_us": sec * 1e6,
+              "work_per_launch": wl.dominant_units,
+              "how": "CUDA events around graph replays of back-to-back launches of this kernel "
+                     "on its launching stream (gaps between graph nodes included)"})
+    return r
+
+
+def secondary_roofline(wl, stream, peaks, reps: int):
+    if not hasattr(wl, "secondary"):
+        return None
+    name, fn, launches, units = wl.secondary()
+    sec = time_launches(fn, stream, reps, launches)
+    r = roofline_of("hbm", units, sec, peaks)
+    r.update({"launch_us": sec * 1e6, "work_per_launch": units})
+    return name, r
+
+
+def run_extras(args, device, stream, peaks) -> dict:
+    """Short passes of the batched, prefill and ingest workloads (one GPU, no e2e, no oracle):
+    value, per-step time, the dominant kernel's roofline and the clocks of each, so that
+    their fractions are measured in the default run.  Each timed region lasts ~1 s."""
+    import torch
+
+    out = {}
+    for name in ("batched", "prefill", "ingest"):
+        wl = WORKLOADS[name](device, args.seed)
+        n_steps, el, units, clk = run_timed(wl, stream, 20, 5, True, 1, device, min_seconds=1.0)
+        entry = {"value": units / el, "unit": "blocks/s", "steps": n_steps,
+                 "ms_per_step": el / n_steps * 1e3, "workload": wl.describe(),
+                 "l2": wl.l2_note, "clocks": clk,
+                 "roofline": dominant_roofline(wl, stream, peaks, 50,
+                                               TRAFFIC.get(name))}
+        sec = secondary_roofline(wl, stream, peaks, 50)
+        if sec is not None:
+            out[sec[0]] = sec[1]
+        out[name] = entry
+        del wl
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_hss(args):
     import torch
 
@@ -934,65 +1112,18 @@ def run_hss(args):
     stream = torch.cuda.Stream(device=device)
     torch.cuda.synchronize()
     per_replay = getattr(wl, "graph_steps", 1)
-    capture = getattr(wl, "steps_for_graph", wl.step)
+    describe, l2_note = wl.describe(), wl.l2_note
+    launches, slot = wl.launches_per_step, wl.slot_bytes()
 
-    # ---- warm-up, then capture the step into a CUDA graph
-    with torch.cuda.stream(stream):
-        for _ in range(max(args.warmup, 3)):
-            capture()
-    stream.synchronize()
-    graph = None
-    if not args.no_graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            capture()
-        for _ in range(3):
-            graph.replay()
-        torch.cuda.synchronize()
-    run_replay = graph.replay if graph is not None else capture
-    replays = max(1, args.steps // per_replay)
-    steps = replays * per_replay
-
-    # ---- timed region
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    barrier(world, device)
-    torch.cuda.synchronize()
-    with ClockSampler(device_uuid(local)) as clocks:
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for _ in range(replays):
-                run_replay()
-            ev1.record(stream)
-        stream.synchronize()
-    torch.cuda.synchronize()
-    barrier(world, device)
-    elapsed = ev0.elapsed_time(ev1) / 1e3
-    elapsed_max, units = aggregate(elapsed, wl.units_per_step * steps, world, device)
+    # ---- timed region: exactly the requested steps
+    steps, elapsed_max, units, clocks = run_timed(wl, stream, args.steps, args.warmup,
+                                                  not args.no_graph, world, device)
     value = units / elapsed_max
 
     # ---- dominant kernel: graphs of back-to-back launches timed with events on its stream
     reps = max(20, min(400, args.steps // 4))
-    g2 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g2, stream=stream):
-        wl.dominant()
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            g2.replay()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(reps):
-            g2.replay()
-        e1.record(stream)
-    stream.synchronize()
-    dom_s = e0.elapsed_time(e1) / 1e3 / (reps * wl.dominant_launches)
-    if wl.dominant_bound == "hbm":
-        achieved, peak, unit = wl.dominant_units / dom_s / 1e9, peaks["hbm_gbs"], "GB/s"
-        peak_src = peaks["source"] + " hbm_gbs (copy)"
-    else:
-        achieved, peak, unit = wl.dominant_units / dom_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
-        peak_src = peaks["source"] + " bf16_tflops (burst, cuBLAS)"
+    roofline = dominant_roofline(wl, stream, peaks, reps, TRAFFIC.get(args.workload))
+    secondary = secondary_roofline(wl, stream, peaks, reps)
 
     # ---- end to end through the API with host buffers
     e2e = None
@@ -1019,6 +1150,18 @@ def run_hss(args):
     if err != 0:
         raise SystemExit(f"device error raised during the benchmark: {hss.status_string(err)}")
 
+    extras = None
+    if args.workload == "decode" and not args.no_extras and world == 1:
+        del wl
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        extras = run_extras(args, device, stream, peaks)
+        err = hss.hss_read_device_error()
+        if err != 0:
+            raise SystemExit(f"device error raised during the extra workloads: "
+                             f"{hss.status_string(err)}")
+        wl = None
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         threads = args.cpu_threads or cpu_threads()
@@ -1030,7 +1173,6 @@ def run_hss(args):
                          f"scored per call in the GPU step's proportions, ~10 s"}
 
     if rank == 0:
-        slot = wl.slot_bytes()
         line = {
             "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": world,
             "steps": steps, "warmup": args.warmup,
@@ -1038,21 +1180,18 @@ def run_hss(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "a_g_gbs": value * slot / 1e9,
             "a_g_hbm_frac": value * slot / 1e9 / peaks["hbm_gbs"],
-            "config": {"workload": wl.describe(), "l2": wl.l2_note, "graph": graph is not None,
+            "config": {"workload": describe, "l2": l2_note, "graph": not args.no_graph,
                        "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": wl.dominant_bound, "kernel": wl.dominant_kernel,
-                         "achieved": achieved, "peak": peak, "unit": unit,
-                         "frac": achieved / peak, "traffic": TRAFFIC[args.workload][0],
-                         "traffic_source": TRAFFIC[args.workload][1], "peak_source": peak_src,
-                         "launch_us": dom_s * 1e6, "work_per_launch": wl.dominant_units,
-                         "how": "CUDA events around graph replays of back-to-back launches of "
-                                "this kernel on its launching stream (gaps between graph nodes "
-                                "included)"},
+            "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": wl.launches_per_step * steps,
-            "clocks": clocks.summary(),
+            "gpu_launches": launches * steps,
+            "clocks": clocks,
         }
+        if secondary is not None:
+            line[secondary[0]] = secondary[1]
+        if extras is not None:
+            line["workloads"] = extras
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -274,7 +274,9 @@ hss_status hss_select_rows(const float* scores, int32_t rows, int64_t num_blocks
  * CTA publishes its blocks' keys in the workspace, waits until the sequence's keys are all
  * there (a bounded wait: HSS_ERR_DEVICE_TIMEOUT after 1 s) and places its own blocks by
  * counting the smaller (score, position) words; otherwise the last CTA to finish a sequence
- * ranks it.
+ * ranks it.  That bounded wait assumes the scoring grid gets the whole GPU: a kernel of
+ * another stream that holds SMs for longer than the limit makes the call report
+ * HSS_ERR_DEVICE_TIMEOUT (its victims are then wrong; zero the workspace before the next call).
  * This is the fused decode call the predictor page's per-step usage implies (module docs
  * of "metrale_storage/predictor.rs": scores only rank eviction victims).
  *
@@ -336,11 +338,14 @@ hss_status hss_layer_step(const hss_dims* dims, const uint16_t* P, const uint16_
  *
  *   Arguments and results: as hss_layer_step, without workspace / workspace_bytes; Qp must
  *   not be NULL here (HSS_ERR_NULL_POINTER).
+ *   Every argument check runs before anything is enqueued, as for the other calls.
  *   num_seqs > HSS_LAYER_STEP_STATIC_MAX_SEQS  -> HSS_ERR_WORKSPACE_TOO_SMALL, nothing enqueued.
  *   Each call first clears the counters it uses (a memset on `stream`), then runs the same
  *   kernels as hss_layer_step.
  *   The first call on a device looks up the array's device address (cudaGetSymbolAddress);
- *   make that first call before any stream capture on that device.
+ *   make that first call before any stream capture on that device.  The address is kept
+ *   for the life of the process: after cudaDeviceReset on that device, reload the library
+ *   before calling this again (the same holds for the library's error word).
  *   All calls share the one array: calls that overlap on the GPU (on different streams, or
  *   unordered) race and give wrong victims.  Order them on one stream.
  */

@@ -296,12 +296,13 @@ class LayerStep:
         self._mid3 = (vp(_ptr(block_table)), vp(_ptr(seq_offsets)), i32(int(num_seqs)),
                       i64(int(total_blocks)))
         self._k = i32(int(k))
-        self._tail = (vp(_ptr(workspace)), sz(int(workspace_bytes)), vp(_ptr(dev_status)))
+        self._ws = (vp(_ptr(workspace)), sz(int(workspace_bytes)))
+        self._status = vp(_ptr(dev_status))
 
     def __call__(self, layer: int, K_new, Q, scores, victims, stream=None) -> None:
         st = self._fn(*self._head, _ptr(K_new), *self._mid1, _ptr(Q), *self._mid2, int(layer),
-                      *self._mid3, _ptr(scores), self._k, _ptr(victims), *self._tail,
-                      _stream(stream))
+                      *self._mid3, _ptr(scores), self._k, _ptr(victims), *self._ws,
+                      self._status, _stream(stream))
         _check(st, "hss_layer_step")
 
 

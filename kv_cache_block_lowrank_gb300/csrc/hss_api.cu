@@ -56,6 +56,73 @@ static hss_status check_dims(const hss_dims* d) {
     return HSS_OK;
 }
 
+
+hss_status layer_step_check(const hss_dims* dims, const uint16_t* P, const uint16_t* K_new,
+                            const int32_t* new_ids, int64_t num_new, const uint16_t* Q,
+                            int32_t rows_per_seq, const uint16_t* Qp, const uint16_t* A_g,
+                            int32_t layer, const int32_t* block_table,
+                            const int32_t* seq_offsets, int32_t num_seqs, int64_t total_blocks,
+                            const float* scores, int32_t k, const int32_t* victims,
+                            const void* workspace, size_t workspace_bytes, LayerStepPlan* plan) {
+    hss_status st = check_dims(dims);
+    if (st != HSS_OK) return st;
+    if (layer < 0 || layer >= dims->num_layers) return HSS_ERR_OUT_OF_RANGE;
+    if (num_new < 0 || num_seqs < 0 || total_blocks < 0 || rows_per_seq < 1 ||
+        total_blocks > 0x7FFFFFFF || k < 1 || k > HSS_MAX_VICTIMS)
+        return HSS_ERR_INVALID_ARGUMENT;
+    if (num_seqs == 0 && total_blocks != 0) return HSS_ERR_INVALID_ARGUMENT;
+    if (P == nullptr || A_g == nullptr) return HSS_ERR_NULL_POINTER;
+    if (num_new > 0 && (K_new == nullptr || new_ids == nullptr)) return HSS_ERR_NULL_POINTER;
+    if (num_seqs > 0 && (Q == nullptr || seq_offsets == nullptr || victims == nullptr))
+        return HSS_ERR_NULL_POINTER;
+    if (total_blocks > 0 && (block_table == nullptr || scores == nullptr))
+        return HSS_ERR_NULL_POINTER;
+    if (!aligned16(P) || !aligned16(A_g) || (K_new != nullptr && !aligned16(K_new)) ||
+        (Q != nullptr && !aligned16(Q)) || (Qp != nullptr && !aligned16(Qp)))
+        return HSS_ERR_MISALIGNED;
+    if (num_seqs > 0) {
+        if (workspace == nullptr) return HSS_ERR_NULL_POINTER;
+        if (workspace_bytes < hss_layer_step_workspace_bytes(num_seqs))
+            return HSS_ERR_WORKSPACE_TOO_SMALL;
+        if ((reinterpret_cast<uintptr_t>(workspace) & 3u) != 0) return HSS_ERR_MISALIGNED;
+    }
+    const int64_t rows_per_block = static_cast<int64_t>(dims->block_size) * dims->num_kv_heads;
+    if (num_new > (int64_t{1} << 31) / rows_per_block) return HSS_ERR_INVALID_ARGUMENT;
+    if (static_cast<int64_t>(num_seqs) * rows_per_seq > (int64_t{1} << 40) / dims->num_q_heads)
+        return HSS_ERR_INVALID_ARGUMENT;
+
+    // The scoring path, decided before anything is launched so that an unsupported shape
+    // enqueues nothing.
+    ScoreArgs& a = plan->score;
+    a = ScoreArgs{};
+    a.Qp = Qp;
+    a.rows_per_seq = rows_per_seq;
+    a.A_g = A_g;
+    a.layer_offset_slots = static_cast<int64_t>(layer) * dims->max_blocks;
+    a.max_blocks = dims->max_blocks;
+    a.table = block_table;
+    a.seq_offsets = seq_offsets;
+    a.num_seqs = num_seqs;
+    a.total = total_blocks;
+    a.scores = const_cast<float*>(scores);
+    a.num_q_heads = dims->num_q_heads;
+    a.num_kv_heads = dims->num_kv_heads;
+    a.r = dims->r;
+    a.block_size = dims->block_size;
+    const int64_t nvec =
+        static_cast<int64_t>(rows_per_seq) * (dims->num_q_heads / dims->num_kv_heads);
+    plan->decode = nvec <= 16 && score_decode_supported(a);
+    if (total_blocks > 0 && !plan->decode && !score_tc_supported(a))
+        return HSS_ERR_UNSUPPORTED_SHAPE;
+    // Qp == NULL: the caller does not want the projected queries, and the decode scorer
+    // projects them itself (one launch fewer on the scoring path).
+    plan->inline_q = Qp == nullptr && num_seqs > 0;
+    if (plan->inline_q && total_blocks > 0 &&
+        !(plan->decode && score_decode_inline_supported(a, dims->head_dim)))
+        return HSS_ERR_NULL_POINTER;
+    return HSS_OK;
+}
+
 }  // namespace hss
 
 using namespace hss;
@@ -260,105 +327,60 @@ hss_status hss_layer_step(const hss_dims* dims, const uint16_t* P, const uint16_
                           int32_t num_seqs, int64_t total_blocks, float* scores, int32_t k,
                           int32_t* victims, void* workspace, size_t workspace_bytes,
                           int32_t* dev_status, void* stream) {
-    hss_status st = check_dims(dims);
+    LayerStepPlan plan;
+    hss_status st = layer_step_check(dims, P, K_new, new_ids, num_new, Q, rows_per_seq, Qp, A_g,
+                                     layer, block_table, seq_offsets, num_seqs, total_blocks,
+                                     scores, k, victims, workspace, workspace_bytes, &plan);
     if (st != HSS_OK) return st;
-    if (layer < 0 || layer >= dims->num_layers) return HSS_ERR_OUT_OF_RANGE;
-    if (num_new < 0 || num_seqs < 0 || total_blocks < 0 || rows_per_seq < 1 ||
-        total_blocks > 0x7FFFFFFF || k < 1 || k > HSS_MAX_VICTIMS)
-        return HSS_ERR_INVALID_ARGUMENT;
-    if (num_seqs == 0 && total_blocks != 0) return HSS_ERR_INVALID_ARGUMENT;
-    if (P == nullptr || A_g == nullptr) return HSS_ERR_NULL_POINTER;
-    if (num_new > 0 && (K_new == nullptr || new_ids == nullptr)) return HSS_ERR_NULL_POINTER;
-    if (num_seqs > 0 && (Q == nullptr || seq_offsets == nullptr || victims == nullptr))
-        return HSS_ERR_NULL_POINTER;
-    if (total_blocks > 0 && (block_table == nullptr || scores == nullptr))
-        return HSS_ERR_NULL_POINTER;
-    if (!aligned16(P) || !aligned16(A_g) || (K_new != nullptr && !aligned16(K_new)) ||
-        (Q != nullptr && !aligned16(Q)) || (Qp != nullptr && !aligned16(Qp)))
-        return HSS_ERR_MISALIGNED;
-    if (num_seqs > 0) {
-        if (workspace == nullptr) return HSS_ERR_NULL_POINTER;
-        if (workspace_bytes < hss_layer_step_workspace_bytes(num_seqs))
-            return HSS_ERR_WORKSPACE_TOO_SMALL;
-        if ((reinterpret_cast<uintptr_t>(workspace) & 3u) != 0) return HSS_ERR_MISALIGNED;
-    }
+    const ScoreArgs& a = plan.score;
     const int64_t rows_per_block = static_cast<int64_t>(dims->block_size) * dims->num_kv_heads;
-    if (num_new > (int64_t{1} << 31) / rows_per_block) return HSS_ERR_INVALID_ARGUMENT;
-    if (static_cast<int64_t>(num_seqs) * rows_per_seq > (int64_t{1} << 40) / dims->num_q_heads)
-        return HSS_ERR_INVALID_ARGUMENT;
-
-    // Decide the scoring path before launching anything, so an unsupported shape enqueues
-    // nothing.
-    ScoreArgs a{};
-    a.Qp = Qp;
-    a.rows_per_seq = rows_per_seq;
-    a.A_g = A_g;
-    a.layer_offset_slots = static_cast<int64_t>(layer) * dims->max_blocks;
-    a.max_blocks = dims->max_blocks;
-    a.table = block_table;
-    a.seq_offsets = seq_offsets;
-    a.num_seqs = num_seqs;
-    a.total = total_blocks;
-    a.scores = scores;
-    a.num_q_heads = dims->num_q_heads;
-    a.num_kv_heads = dims->num_kv_heads;
-    a.r = dims->r;
-    a.block_size = dims->block_size;
-    a.dev_status = dev_status;
-    const int64_t nvec =
-        static_cast<int64_t>(rows_per_seq) * (dims->num_q_heads / dims->num_kv_heads);
-    const bool decode = nvec <= 16 && score_decode_supported(a);
-    if (total_blocks > 0 && !decode && !score_tc_supported(a)) return HSS_ERR_UNSUPPORTED_SHAPE;
-    // Qp == NULL: the caller does not want the projected queries, and the decode scorer
-    // projects them itself (one launch fewer on the scoring path).
-    const bool inline_q = Qp == nullptr && num_seqs > 0;
-    if (inline_q && total_blocks > 0 &&
-        !(decode && score_decode_inline_supported(a, dims->head_dim)))
-        return HSS_ERR_NULL_POINTER;
-
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     // 1. one launch projects the query rows and the newly written blocks
-    ProjectArgs q{};
-    q.P = P;
-    q.X = Q;
-    q.num_rows = static_cast<int64_t>(num_seqs) * rows_per_seq * dims->num_q_heads;
-    q.head_dim = dims->head_dim;
-    q.r = dims->r;
-    q.out = Qp;
-    q.block_ids = nullptr;
-    ProjectArgs kv{};
-    kv.P = P;
-    kv.X = K_new;
-    kv.num_rows = num_new * rows_per_block;
-    kv.head_dim = dims->head_dim;
-    kv.r = dims->r;
-    kv.out = A_g;
-    kv.block_ids = new_ids;
-    kv.num_kv_heads = dims->num_kv_heads;
-    kv.block_size = dims->block_size;
-    kv.max_blocks = dims->max_blocks;
-    kv.layer = layer;
-    kv.dev_status = dev_status;
-    if (inline_q) q.num_rows = 0;  // only the new blocks
-    st = launch_project2(q, &kv, s);
-    if (st != HSS_OK || num_seqs == 0) return st;
+    {
+        ProjectArgs q{};
+        q.P = P;
+        q.X = Q;
+        q.num_rows = plan.inline_q ? 0 : static_cast<int64_t>(num_seqs) * rows_per_seq *
+                                             dims->num_q_heads;
+        q.head_dim = dims->head_dim;
+        q.r = dims->r;
+        q.out = Qp;
+        q.block_ids = nullptr;
+        ProjectArgs kv{};
+        kv.P = P;
+        kv.X = K_new;
+        kv.num_rows = num_new * rows_per_block;
+        kv.head_dim = dims->head_dim;
+        kv.r = dims->r;
+        kv.out = A_g;
+        kv.block_ids = new_ids;
+        kv.num_kv_heads = dims->num_kv_heads;
+        kv.block_size = dims->block_size;
+        kv.max_blocks = dims->max_blocks;
+        kv.layer = layer;
+        kv.dev_status = dev_status;
+        st = launch_project2(q, &kv, s);
+        if (st != HSS_OK || num_seqs == 0) return st;
+    }
     // 2. scores, with the ranking fused into the decode scorer where it fits
     bool fused = false;
     if (total_blocks > 0) {
-        if (decode) {
+        ScoreArgs sa = a;
+        sa.dev_status = dev_status;
+        if (plan.decode) {
             // The kernel just before the scorer is this call's projection unless the queries
             // are projected in the scorer and there are no new blocks: then nothing of this
             // call precedes it and it may read nothing before its dependency wait.
-            const bool own_projection = !inline_q || num_new > 0;
+            const bool own_projection = !plan.inline_q || num_new > 0;
             int32_t* ws = static_cast<int32_t*>(workspace);
-            FusedRank fr{ws + kSpreadRegionBytes / 4, ws, victims, k, own_projection, new_ids,
-                         num_new};
+            const FusedRank fr{ws + kSpreadRegionBytes / 4, ws, victims, k, own_projection,
+                               new_ids, num_new};
             // With the queries projected in the scorer, that projection writes only the new
             // slots, so the scorer need not wait for it anywhere else.
             const InlineQ iq{Q, P, dims->head_dim, num_new > 0};
-            st = launch_score_decode(a, s, &fr, &fused, inline_q ? &iq : nullptr);
+            st = launch_score_decode(sa, s, &fr, &fused, plan.inline_q ? &iq : nullptr);
         } else {
-            st = launch_score_tc(a, s);
+            st = launch_score_tc(sa, s);
         }
         if (st != HSS_OK) return st;
     }

@@ -147,4 +147,20 @@ hss_status launch_select_rows(const float* scores, int32_t rows, int64_t n, int6
 hss_status launch_rank_victims(const float* scores, const int32_t* seq_offsets, int32_t num_seqs,
                                int64_t total, int32_t k, int32_t* victims, cudaStream_t stream);
 
+// ------------------------------------------------------------------- layer step
+// Every argument check of hss_layer_step, and the path it takes, decided before anything is
+// enqueued (hss_layer_step and hss_layer_step_static both run it first).
+struct LayerStepPlan {
+    ScoreArgs score;
+    bool decode = false;    // the decode scorer (else the tcgen05 scorer)
+    bool inline_q = false;  // the decode scorer projects the queries (Qp == NULL)
+};
+hss_status layer_step_check(const hss_dims* dims, const uint16_t* P, const uint16_t* K_new,
+                            const int32_t* new_ids, int64_t num_new, const uint16_t* Q,
+                            int32_t rows_per_seq, const uint16_t* Qp, const uint16_t* A_g,
+                            int32_t layer, const int32_t* block_table,
+                            const int32_t* seq_offsets, int32_t num_seqs, int64_t total_blocks,
+                            const float* scores, int32_t k, const int32_t* victims,
+                            const void* workspace, size_t workspace_bytes, LayerStepPlan* plan);
+
 }  // namespace hss

@@ -26,7 +26,9 @@ constexpr int kStaticWords = kStaticMaxSeqs + 64 + 2 * 4096;
 static __device__ __align__(256) int32_t g_static_counters[kStaticWords];
 
 // Device address of g_static_counters, looked up once per device with that device current
-// (the symbol's name in host code is only a stand-in, not an address a kernel can use).
+// (the symbol's name in host code is only a stand-in, not an address a kernel can use).  It
+// is kept for the life of the process: cudaDeviceReset unloads the module, so a caller that
+// resets a device reloads the library before the next call on it.
 constexpr int kMaxDevices = 64;
 int32_t* g_counters_addr[kMaxDevices] = {nullptr};
 std::mutex g_counters_mu;
@@ -66,23 +68,18 @@ hss_status hss_layer_step_static(const hss_dims* dims, const uint16_t* P, const 
                               block_table, seq_offsets, num_seqs, total_blocks, scores, k,
                               victims, nullptr, 0, dev_status, stream);
     }
-    // The argument checks that can fail come before anything is enqueued (hss_layer_step
-    // repeats them all).
-    hss_status st = hss_validate_dims(dims);
+    if (Qp == nullptr) return HSS_ERR_NULL_POINTER;
+    // Every check hss_layer_step makes comes first, so that a call that fails enqueues
+    // nothing, not even the clear.  The array is 256-byte aligned and large enough, so its
+    // own checks pass for any address of that alignment; the check never dereferences it.
+    const size_t bytes = static_cast<size_t>(kStaticWords) * sizeof(int32_t);
+    LayerStepPlan plan;
+    hss_status st = layer_step_check(dims, P, K_new, new_ids, num_new, Q, rows_per_seq, Qp, A_g,
+                                     layer, block_table, seq_offsets, num_seqs, total_blocks,
+                                     scores, k, victims, reinterpret_cast<const void*>(256),
+                                     bytes, &plan);
     if (st != HSS_OK) return st;
-    if (layer < 0 || layer >= dims->num_layers) return HSS_ERR_OUT_OF_RANGE;
-    if (num_new < 0 || total_blocks < 0 || rows_per_seq < 1 || total_blocks > 0x7FFFFFFF ||
-        k < 1 || k > HSS_MAX_VICTIMS)
-        return HSS_ERR_INVALID_ARGUMENT;
-    if (P == nullptr || A_g == nullptr || Q == nullptr || Qp == nullptr ||
-        seq_offsets == nullptr || victims == nullptr ||
-        (num_new > 0 && (K_new == nullptr || new_ids == nullptr)) ||
-        (total_blocks > 0 && (block_table == nullptr || scores == nullptr)))
-        return HSS_ERR_NULL_POINTER;
-    const uintptr_t mis = reinterpret_cast<uintptr_t>(P) | reinterpret_cast<uintptr_t>(A_g) |
-                          reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(Qp) |
-                          reinterpret_cast<uintptr_t>(K_new);
-    if ((mis & 15u) != 0) return HSS_ERR_MISALIGNED;
+    // The array's address (a host-side lookup; nothing is enqueued).
     int32_t* counters = nullptr;
     st = counters_for_current_device(&counters);
     if (st != HSS_OK) return st;
@@ -94,8 +91,7 @@ hss_status hss_layer_step_static(const hss_dims* dims, const uint16_t* P, const 
         return HSS_ERR_CUDA;
     return hss_layer_step(dims, P, K_new, new_ids, num_new, Q, rows_per_seq, Qp, A_g, layer,
                           block_table, seq_offsets, num_seqs, total_blocks, scores, k, victims,
-                          counters, static_cast<size_t>(kStaticWords) * sizeof(int32_t),
-                          dev_status, stream);
+                          counters, bytes, dev_status, stream);
 }
 
 }  // extern "C"

@@ -23,6 +23,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <type_traits>
 
 #include "rank_device.cuh"
 
@@ -92,7 +93,17 @@ struct DecodeParams {
     // word of the sequence carries this call's tag and places its own entries by counting the
     // smaller words, so the ranking is spread over the grid.
     int32_t spread;
+    // TMA kernels (INLINE, at most 2 entries per warp, slots of at most 8 KiB): each warp's
+    // slots arrive by one bulk copy per entry into its shared-memory buffer, completion counted
+    // on the warp's mbarrier, instead of through the warp's own loads.  Offsets of the eight
+    // mbarriers and of the eight slot buffers in shared memory.
+    int32_t tma_bar_off;
+    int32_t tma_buf_off;
 };
+
+// TMA slot buffers: the largest slot and the most entries per warp they take.
+constexpr int kTmaMaxSlotBytes = 8192;
+constexpr int kTmaMaxEntriesPerWarp = 2;
 
 // Spread ranking: keys per thread (256 threads) and so the longest sequence it takes.
 constexpr int kSpreadKeysPerThread = 16;
@@ -177,7 +188,8 @@ __device__ __forceinline__ int frag_r_offset(int ks, int t) {
 
 // MASKED: the call passed ctx_len or row_pos0.  A template parameter, so the unmasked kernel
 // carries none of the mask arithmetic.  INLINE: the queries are projected in the kernel.
-template <int KSTEPS, int NT, bool MASKED, bool INLINE>
+// TMA: slots arrive by bulk copies into shared memory (INLINE kernels only).
+template <int KSTEPS, int NT, bool MASKED, bool INLINE, bool TMA>
 __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(16) uint8_t smem_dec[];
     uint2* frag_cache_all = reinterpret_cast<uint2*>(smem_dec);
@@ -202,9 +214,12 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
     const int64_t slot_elems = static_cast<int64_t>(p.nkv) * p.bs * p.r;
     const int64_t tile_elems = 16 * static_cast<int64_t>(p.r);
 
-    // One batch of a slot's 16-token tiles, straight into MMA A-fragment registers.
+    // One batch of a slot's 16-token tiles, straight into MMA A-fragment registers, from
+    // global memory (streaming loads) or from the slot's copy in shared memory (TMA kernels;
+    // the same layout).
     uint32_t data[kTilesPerBatch][kRegsPerTile];
-    auto issue_loads = [&](const uint16_t* slot, int tb) {
+    auto issue_loads_from = [&](const uint16_t* slot, int tb, auto in_smem) {
+        constexpr bool kSmem = decltype(in_smem)::value;
 #pragma unroll
         for (int u = 0; u < kTilesPerBatch; ++u) {
             const int tile = tb + u;
@@ -216,12 +231,13 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
 #pragma unroll
                     for (int l = 0; l < kLoadsPerRow; ++l) {
                         if constexpr (KSTEPS == 1) {
-                            const uint2 v = __ldcs(reinterpret_cast<const uint2*>(rowp + 4 * tq));
+                            const uint2* src = reinterpret_cast<const uint2*>(rowp + 4 * tq);
+                            const uint2 v = kSmem ? *src : __ldcs(src);
                             data[u][half * 2 + 0] = v.x;
                             data[u][half * 2 + 1] = v.y;
                         } else {
-                            const uint4 v =
-                                __ldcs(reinterpret_cast<const uint4*>(rowp + 32 * l + 8 * tq));
+                            const uint4* src = reinterpret_cast<const uint4*>(rowp + 32 * l + 8 * tq);
+                            const uint4 v = kSmem ? *src : __ldcs(src);
                             data[u][(half * kLoadsPerRow + l) * 4 + 0] = v.x;
                             data[u][(half * kLoadsPerRow + l) * 4 + 1] = v.y;
                             data[u][(half * kLoadsPerRow + l) * 4 + 2] = v.z;
@@ -232,6 +248,36 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
             }
         }
     };
+    auto issue_loads = [&](const uint16_t* slot, int tb) {
+        issue_loads_from(slot, tb, std::false_type{});
+    };
+    // TMA kernels: the warp's slot buffer and its mbarrier.  A slot's copy is started by lane 0
+    // (expect the bytes, then one bulk copy); the warp waits on the barrier's current phase
+    // before it reads the buffer.  Issuing 8 KiB of per-lane loads per warp kept the SM's load
+    // queue busy for ~1 us, and every shared-memory access issued after them waited behind
+    // them; the bulk copies bypass that queue.
+    uint64_t* tma_bar = reinterpret_cast<uint64_t*>(smem_dec + p.tma_bar_off) + warp;
+    uint16_t* tma_buf = reinterpret_cast<uint16_t*>(smem_dec + p.tma_buf_off) + warp * slot_elems;
+    uint32_t tma_parity = 0;
+    const uint32_t slot_bytes = static_cast<uint32_t>(slot_elems * 2);
+    auto tma_start = [&](int32_t id) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(tma_bar, slot_bytes);
+            bulk_copy_g2s(tma_buf, p.A_g + (p.layer_slots + id) * slot_elems, slot_bytes, tma_bar);
+        }
+    };
+    // Issue a slot's data: loads into the registers, or (TMA) the bulk copy.
+    auto start_slot = [&](int32_t id) {
+        if constexpr (TMA)
+            tma_start(id);
+        else
+            issue_loads(p.A_g + (p.layer_slots + id) * slot_elems, 0);
+    };
+    if constexpr (TMA) {
+        if (lane == 0) mbar_init(tma_bar, 1);
+        fence_mbarrier_init();
+        __syncwarp();
+    }
     // The last s with seq_offsets[s] <= i, searched 32 ways at a time: each round the lanes
     // load 32 evenly spaced offsets of the range at once (one L2 round trip for up to 32
     // sequences, two for up to 1024).  Whole warp.
@@ -251,13 +297,47 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
     int s = 0;
     int64_t seq_end = 0;
     int32_t my_id = 0;
+    bool have_ids = false;  // my_id already holds the first batch's entries
     bool preloaded = false;
+    // INLINE: the staging loads (Q's rows by asynchronous copies, P's first two pieces per
+    // thread into registers) are requested before any slot data: Q of a layer is touched once
+    // per model step and comes from DRAM, where it queued behind the 16 MiB of slot traffic
+    // (~3 us) when it was requested after it.
+    uint4* pfrag = reinterpret_cast<uint4*>(smem_dec + p.cache_bytes);
+    uint16_t* pfrag_h = reinterpret_cast<uint16_t*>(pfrag);
+    uint16_t* qs = reinterpret_cast<uint16_t*>(smem_dec + p.cache_bytes + p.r * p.hd * 2);
+    const int qstride = p.hd + 32;  // padded rows: conflict-free fragment reads
+    const int qvec = p.hd >> 3;
+    const int pvec = p.r >> 3;  // 16-byte pieces per row of P: 2, 4, 8 or 16
+    const int pshift = __ffs(pvec) - 1;
+    const int p_items = p.hd * pvec;
+    uint4 pv[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+    bool staged = false;
+    auto stage_issue = [&]() {
+        for (int z = threadIdx.x; z < p.cache_bytes / 16; z += blockDim.x)
+            reinterpret_cast<uint4*>(smem_dec)[z] = make_uint4(0u, 0u, 0u, 0u);
+        const int M = p.rows * p.nq;
+        for (int e = threadIdx.x; e < p.num_seqs * M * qvec; e += blockDim.x) {
+            const int row = e / qvec, c8 = e - row * qvec;
+            cp_async_16(qs + row * qstride + 8 * c8, p.Q + static_cast<int64_t>(row) * p.hd + 8 * c8);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int e = static_cast<int>(threadIdx.x) + u * static_cast<int>(blockDim.x);
+            const int dd = e >> pshift, jc = e & (pvec - 1);
+            if (e < p_items) pv[u] = __ldg(reinterpret_cast<const uint4*>(p.P + dd * p.r) + jc);
+        }
+        staged = true;
+    };
+    if (INLINE && p.early) stage_issue();  // the previous kernel writes neither Q nor P
+
     if (p.early && has_work) {
         // The previous kernel in the stream is this call's own projection, which writes only
         // Qp and the slots of new_ids: the offsets, the table and every other slot may be
         // read before the dependency wait, so the first block's DRAM latency overlaps it.
         const int64_t first_n = i_end - i_begin < 32 ? i_end - i_begin : 32;
         my_id = lane < first_n ? __ldg(&p.table[i_begin + lane]) : 0;
+        have_ids = true;
         // num_new <= 64: two new ids per lane, loaded alongside the table entries.
         const int32_t nid0 = lane < p.num_new ? __ldg(&p.new_ids[lane]) : -1;
         const int32_t nid1 = lane + 32 < p.num_new ? __ldg(&p.new_ids[lane + 32]) : -1;
@@ -266,7 +346,7 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
         const int32_t id0 = __shfl_sync(0xffffffffu, my_id, 0);
         const bool fresh = __any_sync(0xffffffffu, nid0 == id0 || nid1 == id0);
         if (id0 >= 0 && id0 < p.max_blocks && !fresh) {
-            issue_loads(p.A_g + (p.layer_slots + id0) * slot_elems, 0);
+            start_slot(id0);
             preloaded = true;
         }
     }
@@ -280,54 +360,32 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
     bool waited = !nowait;
 
     if constexpr (INLINE) {
+        if (!staged) stage_issue();
         // The first block's loads go out before the projection below, so their DRAM latency
         // covers it (without this call's own projection before the scorer they could not be
         // issued before the dependency wait).
         if (has_work && !preloaded) {
             const int64_t first_n = i_end - i_begin < 32 ? i_end - i_begin : 32;
             my_id = lane < first_n ? __ldg(&p.table[i_begin + lane]) : 0;
+            have_ids = true;
             s = find_seq(i_begin);
             seq_end = __ldg(&p.seq_offsets[s + 1]);
             const int32_t id0 = __shfl_sync(0xffffffffu, my_id, 0);
             if (id0 >= 0 && id0 < p.max_blocks && !__any_sync(0xffffffffu, my_new == id0)) {
-                issue_loads(p.A_g + (p.layer_slots + id0) * slot_elems, 0);
+                start_slot(id0);
                 preloaded = true;
             }
         }
         // ---- project every sequence's queries into the CTA's fragment cache
-        // Staging, one coalesced round trip: P as MMA B fragments and Q's rows.  The
-        // head_dim coordinates are visited in the order that makes each lane's 16-byte load
-        // of a query row its A fragment for two k-steps (the scheme the slot loads use for
-        // r), so B takes the same order: fragment entry (n-tile np, 32-wide chunk l, lane)
-        // holds P[32l + 8t + e][8np + g] as its e-th bf16 (t = lane % 4, g = lane / 4).
-        uint4* pfrag = reinterpret_cast<uint4*>(smem_dec + p.cache_bytes);
-        uint16_t* pfrag_h = reinterpret_cast<uint16_t*>(pfrag);
-        uint16_t* qs = reinterpret_cast<uint16_t*>(smem_dec + p.cache_bytes + p.r * p.hd * 2);
-        const int qstride = p.hd + 32;  // padded rows: conflict-free fragment reads
+        // P goes to shared memory as MMA B fragments.  The head_dim coordinates are visited in
+        // the order that makes each lane's 16-byte load of a query row its A fragment for two
+        // k-steps (the scheme the slot loads use for r), so B takes the same order: fragment
+        // entry (n-tile np, 32-wide chunk l, lane) holds P[32l + 8t + e][8np + g] as its e-th
+        // bf16 (t = lane % 4, g = lane / 4).  Pieces past the first two per thread are loaded
+        // two at a time here.
         const int lchunks = p.hd >> 5;
         const int M = p.rows * p.nq;
-        for (int z = threadIdx.x; z < p.cache_bytes / 16; z += blockDim.x)
-            reinterpret_cast<uint4*>(smem_dec)[z] = make_uint4(0u, 0u, 0u, 0u);
-        // Q's rows go to shared memory by asynchronous copies (no registers); P's 16-byte
-        // pieces are loaded two per thread before either is scattered, so the staging costs
-        // one L2 round trip when the pieces are at most two per thread.
-        const int qvec = p.hd >> 3;
-        for (int e = threadIdx.x; e < p.num_seqs * M * qvec; e += blockDim.x) {
-            const int row = e / qvec, c8 = e - row * qvec;
-            cp_async_16(qs + row * qstride + 8 * c8, p.Q + static_cast<int64_t>(row) * p.hd + 8 * c8);
-        }
-        const int pvec = p.r >> 3;  // 16-byte pieces per row of P: 2, 4, 8 or 16
-        const int pshift = __ffs(pvec) - 1;
-        const int p_items = p.hd * pvec;
-        for (int e0 = threadIdx.x; e0 < p_items; e0 += 2 * static_cast<int>(blockDim.x)) {
-            uint4 v[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int e = e0 + u * static_cast<int>(blockDim.x);
-                const int dd = e >> pshift, jc = e & (pvec - 1);
-                v[u] = e < p_items ? __ldg(reinterpret_cast<const uint4*>(p.P + dd * p.r) + jc)
-                                   : make_uint4(0u, 0u, 0u, 0u);
-            }
+        auto scatter_p = [&](const uint4 (&v)[2], int e0) {
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int e = e0 + u * static_cast<int>(blockDim.x);
@@ -342,6 +400,19 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
                             static_cast<uint16_t>(w[jj >> 1] >> ((jj & 1) * 16));
                 }
             }
+        };
+        scatter_p(pv, static_cast<int>(threadIdx.x));
+        for (int e0 = static_cast<int>(threadIdx.x) + 2 * static_cast<int>(blockDim.x);
+             e0 < p_items; e0 += 2 * static_cast<int>(blockDim.x)) {
+            uint4 v[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int e = e0 + u * static_cast<int>(blockDim.x);
+                const int dd = e >> pshift, jc = e & (pvec - 1);
+                v[u] = e < p_items ? __ldg(reinterpret_cast<const uint4*>(p.P + dd * p.r) + jc)
+                                   : make_uint4(0u, 0u, 0u, 0u);
+            }
+            scatter_p(v, e0);
         }
         cp_async_wait_all();
         __syncthreads();
@@ -429,7 +500,7 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
     for (int64_t i0 = i_begin; i0 < i_end; i0 += 32) {
         const int64_t left = i_end - i0;
         const int n_here = left < 32 ? static_cast<int>(left) : 32;
-        if (!(p.early && i0 == i_begin)) my_id = lane < n_here ? __ldg(&p.table[i0 + lane]) : 0;
+        if (!(have_ids && i0 == i_begin)) my_id = lane < n_here ? __ldg(&p.table[i0 + lane]) : 0;
         for (int e = 0; e < n_here; ++e) {
             const int64_t i = i0 + e;
             while (i >= seq_end && s + 1 < p.num_seqs) {
@@ -455,10 +526,28 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
                 waited = true;
             }
             const uint16_t* slot = p.A_g + (p.layer_slots + id) * slot_elems;
+            if constexpr (TMA) {
+                // The buffer holds one slot: the previous entry's reads are done (and ordered
+                // before the async proxy's writes) before the next copy starts.
+                if (!(preloaded && i == i_begin)) {
+                    __syncwarp();
+                    fence_proxy_async_smem();
+                    tma_start(id);
+                }
+                if (!mbar_wait(tma_bar, tma_parity)) {
+                    // Bounded: a copy that has not landed in 1 s is reported, not waited for.
+                    if (lane == 0) raise_error(p.dev_status, p.lib_error, HSS_ERR_DEVICE_TIMEOUT);
+                }
+                tma_parity ^= 1u;
+                slot = tma_buf;
+            }
             float best = -INFINITY;
             for (int tb = 0; tb < num_tiles; tb += kTilesPerBatch) {
                 // Issue every load of the batch first (the first one may already be in flight).
-                if (!(preloaded && i == i_begin && tb == 0)) issue_loads(slot, tb);
+                if constexpr (TMA)
+                    issue_loads_from(slot, tb, std::true_type{});
+                else if (!(preloaded && i == i_begin && tb == 0))
+                    issue_loads(slot, tb);
                 // (Re)fill the query-vector fragment cache while the loads are in flight.
                 if (INLINE && s != cached_seq) {
                     cache = frag_cache_all + s * frag_per_warp;  // the CTA's projection
@@ -761,17 +850,19 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
 template <int KSTEPS, int NT>
 auto kernel_for(const DecodeParams& p) {
     const bool masked = p.ctx_len != nullptr || p.row_pos0 != nullptr;
-    return p.Q != nullptr ? score_decode_kernel<KSTEPS, NT, false, true>
-           : masked       ? score_decode_kernel<KSTEPS, NT, true, false>
-                          : score_decode_kernel<KSTEPS, NT, false, false>;
+    return p.Q != nullptr && p.tma_buf_off != 0 ? score_decode_kernel<KSTEPS, NT, false, true, true>
+           : p.Q != nullptr ? score_decode_kernel<KSTEPS, NT, false, true, false>
+           : masked         ? score_decode_kernel<KSTEPS, NT, true, false, false>
+                            : score_decode_kernel<KSTEPS, NT, false, false, false>;
 }
 
 // CTAs of 256 threads with `smem` bytes of dynamic shared memory that one SM holds at once,
 // for the kernel `p` selects (cached per kernel: the last shared-memory size asked for).
 template <int KSTEPS, int NT>
 int ctas_per_sm_t(const DecodeParams& p, int smem) {
-    static std::atomic<uint64_t> cache[3];  // (smem << 32 | ctas) per kernel of kernel_for
-    const int which = p.Q != nullptr ? 0 : (p.ctx_len != nullptr || p.row_pos0 != nullptr) ? 1 : 2;
+    static std::atomic<uint64_t> cache[4];  // (smem << 32 | ctas) per kernel of kernel_for
+    const int which = p.Q != nullptr ? (p.tma_buf_off != 0 ? 3 : 0)
+                      : (p.ctx_len != nullptr || p.row_pos0 != nullptr) ? 1 : 2;
     const uint64_t c = cache[which].load(std::memory_order_relaxed);
     if (c != 0 && static_cast<int>(c >> 32) == smem) return static_cast<int>(c & 0xFFFFFFFFu);
     auto k = kernel_for<KSTEPS, NT>(p);
@@ -874,6 +965,8 @@ hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream, const Fu
     p.hd = 0;
     p.cache_bytes = 0;
     p.nowait = 0;
+    p.tma_bar_off = 0;
+    p.tma_buf_off = 0;
     if (fr != nullptr && fr->early && fr->num_new <= 64) {
         p.new_ids = fr->new_ids;
         p.num_new = static_cast<int32_t>(fr->num_new);
@@ -893,10 +986,25 @@ hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream, const Fu
         warps_per_cta = kWarpsMax;
         smem = static_cast<int>(inline_bytes(a, iq->head_dim));
     }
-    p.frag_bytes_cta = smem;
     // Enough warps for two CTAs per SM; each warp takes a contiguous run of entries.
     const int64_t target_warps = static_cast<int64_t>(dev->num_sms) * 2 * warps_per_cta;
     p.entries_per_warp = std::max<int64_t>(1, (a.total + target_warps - 1) / target_warps);
+    // Queries projected in the scorer, at most two entries per warp and small slots: the
+    // slots come by bulk copies into one shared buffer per warp (eight mbarriers, then the
+    // buffers on 128-byte boundaries), if that still leaves room for two CTAs per SM.
+    const int64_t slot_bytes = static_cast<int64_t>(a.num_kv_heads) * a.block_size * a.r * 2;
+    if (iq != nullptr && p.entries_per_warp <= kTmaMaxEntriesPerWarp &&
+        slot_bytes <= kTmaMaxSlotBytes) {
+        const int bar_off = (smem + 15) / 16 * 16;
+        const int buf_off = (bar_off + 8 * kWarpsMax + 127) / 128 * 128;
+        const int end = buf_off + kWarpsMax * static_cast<int>(slot_bytes);
+        if (end + 8 * 1024 <= dev->max_smem_optin / 2) {
+            p.tma_bar_off = bar_off;
+            p.tma_buf_off = buf_off;
+            smem = end;
+        }
+    }
+    p.frag_bytes_cta = smem;
     const int64_t warps = (a.total + p.entries_per_warp - 1) / p.entries_per_warp;
     const int grid = static_cast<int>((warps + warps_per_cta - 1) / warps_per_cta);
     // The ranking can ride along when a whole CTA of 8 warps is there to run it, every

@@ -89,9 +89,9 @@ def test_a_g_bytes(lib):
 FAKE = 0x10000  # never dereferenced: every call below fails validation first
 
 
-def status_of(fn, *args):
+def status_of(fn, *args, **kw):
     with pytest.raises(hss.HssError) as e:
-        fn(*args)
+        fn(*args, **kw)
     return e.value.status
 
 
@@ -184,6 +184,23 @@ def test_layer_step_validation(lib):
     assert status_of(hss.hss_layer_step, *qnull(S=9)) == hss.HSS_ERR_NULL_POINTER
     wide = dims(num_q_heads=64, num_kv_heads=2)  # 32 query vectors per kv head: tcgen05 path
     assert status_of(hss.hss_layer_step, *qnull(d=wide)) == hss.HSS_ERR_NULL_POINTER
+
+
+def test_static_layer_step_checks_before_anything(lib):
+    # The allocation-free variant runs every check of hss_layer_step before it looks up its
+    # array or enqueues the clear: the same statuses come back on a machine without a GPU.
+    base = lambda **o: [o.get("d", dims()), FAKE, FAKE, FAKE, o.get("num_new", 1), FAKE, 1,
+                        o.get("Qp", FAKE), FAKE, o.get("layer", 0), FAKE, FAKE, o.get("S", 1), 10,
+                        FAKE, o.get("k", 4), FAKE, None, 0]
+    st = lambda **o: status_of(hss.hss_layer_step_static, *base(**o))
+    assert st(layer=99) == hss.HSS_ERR_OUT_OF_RANGE
+    assert st(k=0) == hss.HSS_ERR_INVALID_ARGUMENT
+    assert st(num_new=-1) == hss.HSS_ERR_INVALID_ARGUMENT
+    assert st(Qp=None) == hss.HSS_ERR_NULL_POINTER
+    assert st(d=dims(num_kv_heads=3)) == hss.HSS_ERR_INVALID_DIMS
+    assert st(S=hss.hss_layer_step_static_max_seqs() + 1) == hss.HSS_ERR_WORKSPACE_TOO_SMALL
+    wide = dims(num_q_heads=64, num_kv_heads=2, head_dim=128, r=16, block_size=48)
+    assert st(d=wide) == hss.HSS_ERR_UNSUPPORTED_SHAPE  # tcgen05 path: block size 16 or 32
 
 
 def test_self_test_validation(lib):

@@ -6,7 +6,8 @@ import torch
 import kv_cache_block_lowrank_gb300 as hss
 import oracle
 import workloads as W
-from gpu_util import assert_scores_close, assert_victims_match, bits
+from gpu_util import (assert_bf16_within_ulp, assert_scores_close, assert_victims_match, bits,
+                      slot_scale_fn)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -128,9 +129,21 @@ def test_layer_step_against_oracle():
     assert_victims_match(vic.cpu().numpy(), s_o, t_o, case.seq_offsets.numpy(), 8, gpu_scores=s_g)
 
 
-def inline_vs_oracle(d, x, layer, k):
-    """hss_layer_step with Qp = NULL (queries projected inside the scorer) against the
-    oracle; the new slots must equal the projection kernel's, bit for bit."""
+def oracle_new_slots(d, x, layer):
+    """The caller's A_g with the oracle's projection of this call's new blocks written in."""
+    A_o = bits(x["A"].cpu()).copy()
+    if x["n_new"]:
+        st = oracle.project_kv_blocks(bits(x["P"].cpu()), bits(x["K_new"][:x["n_new"]].cpu()),
+                                      layer, x["new_ids"].cpu().numpy(), A_o, nthreads=8)
+        assert st == 0 or x.get("bad_new", False)
+    return A_o
+
+
+def inline_vs_oracle(d, x, layer, k, status=0):
+    """hss_layer_step with Qp = NULL (queries projected inside the scorer) against the oracle:
+    the new slots within 1 bf16 ulp of the oracle's, every other slot untouched, scores within
+    tolerance, victims exact outside the tolerance band and exactly the ranking kernel's order
+    of the call's own scores."""
     A = x["A"].clone()
     sc = torch.empty(x["total"], dtype=torch.float32, device=DEV)
     vic = torch.full((x["S"], k), 12345, dtype=torch.int32, device=DEV)
@@ -140,19 +153,30 @@ def inline_vs_oracle(d, x, layer, k):
     hss.hss_layer_step(d, x["P"], x["K_new"], x["new_ids"], x["n_new"], x["Q"], x["rows"], None,
                        A, layer, x["table"], x["offs"], x["S"], x["total"], sc, k, vic, ws, nb, st)
     torch.cuda.synchronize()
-    assert int(st.item()) == 0
+    assert int(st.item()) == status
     assert counters_zero(ws, x["S"]), "the counters must be left zeroed"
-    A_ref, _, _, _ = separate(d, x, layer, k)
-    assert torch.equal(A.view(torch.int16), A_ref.view(torch.int16))
+    A_o = oracle_new_slots(d, x, layer)
+    A_g = bits(A.cpu())
+    new = x["new_ids"].cpu().numpy()[:x["n_new"]]
+    new = new[(new >= 0) & (new < d.max_blocks)]
+    keep = np.ones(d.max_blocks, dtype=bool)
+    keep[new] = False
+    assert np.array_equal(A_g[layer][keep], A_o[layer][keep]), "wrote a slot that is not new"
+    assert np.array_equal(np.delete(A_g, layer, axis=0), np.delete(A_o, layer, axis=0))
+    if new.size:
+        pos = [int(np.nonzero(x["new_ids"].cpu().numpy() == b)[0][0]) for b in new]
+        scale = slot_scale_fn(x["K_new"][torch.as_tensor(pos)], x["P"])
+        assert_bf16_within_ulp(A_g[layer][new], A_o[layer][new], what="new slots", scale=scale,
+                               n_terms=d.head_dim)
     Qp_o = oracle.project_q(bits(x["Q"].cpu()).reshape(-1, d.num_q_heads, d.head_dim),
                             bits(x["P"].cpu()))
     Qp_o = Qp_o.reshape(x["S"], x["rows"], d.num_q_heads, d.r)
     offs = x["offs"].cpu().numpy().astype(np.int64)
-    s_o, t_o, _ = oracle.score_blocks(Qp_o, bits(A_ref.cpu()), layer, x["table"].cpu().numpy(),
-                                      offs)
+    s_o, t_o, _ = oracle.score_blocks(Qp_o, A_o, layer, x["table"].cpu().numpy(), offs)
     s_g = sc.cpu().numpy()
     assert_scores_close(s_g, s_o, t_o)
     assert_victims_match(vic.cpu().numpy(), s_o, t_o, offs, k, gpu_scores=s_g)
+    return A, sc, vic
 
 
 @pytest.mark.parametrize("shape,lengths,rows,n_new,k", [
@@ -171,14 +195,36 @@ def test_layer_step_inline_query_projection(shape, lengths, rows, n_new, k):
 
 
 def test_layer_step_inline_new_block_outside_the_table():
-    # A new block that no table entry names is still written; the scorer waits for the
-    # projection only where it reads a new block.
+    # A new block that no table entry names is still written; only the new slots change.
     d = W.Dims(1, 32, 8, 128, 32, 16, 600)
     x = make(d, [500], 1, 2, seed=99)
     in_table = set(x["table"].tolist())
     outside = next(b for b in range(d.max_blocks) if b not in in_table)
     x["new_ids"] = torch.tensor([int(x["table"][7]), outside], dtype=torch.int32, device=DEV)
     inline_vs_oracle(d, x, 0, 32)
+
+
+@pytest.mark.parametrize("first,n_new", [(8, 3), (2040, 2), (0, 8), (100, 9)])
+def test_layer_step_several_new_blocks(first, n_new):
+    # The decode layer (8 table entries per scoring CTA): n_new new blocks at consecutive
+    # table positions, so several warps of one CTA wait for the projection of their block.
+    d = W.Dims(2, 32, 8, 128, 32, 16, 2100)
+    x = make(d, [2048], 1, n_new, seed=first + n_new)
+    x["new_ids"] = x["table"][first:first + n_new].contiguous()
+    x["K_new"] = W.bf16_normal(torch.Generator().manual_seed(first),
+                               (n_new, 16, 8, 128)).to(DEV)
+    inline_vs_oracle(d, x, 1, 256)
+
+
+def test_layer_step_bad_new_id():
+    # A new id outside the pool is skipped and reported; the call's other results stand.
+    d = W.Dims(1, 32, 8, 128, 32, 16, 2100)
+    x = make(d, [2048], 1, 2, seed=31)
+    x["new_ids"] = torch.tensor([int(x["table"][5]), d.max_blocks + 7], dtype=torch.int32,
+                                device=DEV)
+    x["bad_new"] = True
+    inline_vs_oracle(d, x, 0, 256, status=hss.HSS_ERR_OUT_OF_RANGE)
+    assert hss.hss_read_device_error() == hss.HSS_ERR_OUT_OF_RANGE
 
 
 def _with_ties(x, d, groups, seed):
@@ -228,8 +274,18 @@ def test_layer_step_one_sequence_ranking(shape, n, k, ties, inline):
         torch.cuda.synchronize()
         assert int(st.item()) == 0
         assert counters_zero(ws, 1), "the counters must be left zeroed"
-        assert torch.equal(sc, sc1)
-        assert torch.equal(vic, vic1)
+        if inline:
+            # The scorer projected the queries and the new block itself (within 1 ulp of the
+            # separate projections): its ranking must be exactly the ranking kernel's on the
+            # call's own scores, and the scores stay within the score tolerance.
+            ref = torch.empty(1, k, dtype=torch.int32, device=DEV)
+            hss.hss_rank_victims(sc, x["offs"], 1, n, k, ref)
+            torch.cuda.synchronize()
+            assert torch.equal(vic, ref)
+            assert torch.allclose(sc, sc1, rtol=2e-3, atol=1e-2)
+        else:
+            assert torch.equal(sc, sc1)
+            assert torch.equal(vic, vic1)
     if ties:
         s = sc1.cpu().numpy()
         assert len(np.unique(s)) <= ties

@@ -98,3 +98,50 @@ def test_static_limit_is_enforced():
                                   0x10000, 0x10000, limit + 1, limit + 1, 0x10000, 4, 0x10000,
                                   None, 0)
     assert e.value.status == hss.HSS_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_static_null_qp_is_rejected():
+    # This entry point needs the caller's Qp buffer; NULL comes back as an error, not a launch.
+    dims = W.Dims(2, 32, 8, 128, 32, 16, 2100)
+    x = inputs(dims, [2048], 1, 1, seed=3)
+    A, _, sc, vic = outputs(dims, x, 256)
+    with pytest.raises(hss.HssError) as e:
+        hss.hss_layer_step_static(dims, x["P"], x["K_new"], x["new_ids"], 1, x["Q"], 1, None, A,
+                                  0, x["table"], x["offs"], 1, x["total"], sc, 256, vic)
+    assert e.value.status == hss.HSS_ERR_NULL_POINTER
+
+
+def test_static_failed_call_then_valid_call():
+    # A call that fails its checks enqueues nothing; the valid call after it is still exact.
+    dims = W.Dims(2, 32, 8, 128, 32, 16, 2100)
+    x = inputs(dims, [2048], 1, 1, seed=5)
+    A, Qp, sc, vic = outputs(dims, x, 256)
+    with pytest.raises(hss.HssError) as e:  # layer out of range
+        hss.hss_layer_step_static(dims, x["P"], x["K_new"], x["new_ids"], 1, x["Q"], 1, Qp, A, 7,
+                                  x["table"], x["offs"], 1, x["total"], sc, 256, vic)
+    assert e.value.status == hss.HSS_ERR_OUT_OF_RANGE
+    torch.cuda.synchronize()
+    assert (vic == 777).all(), "a failed call must not have run anything"
+    ref = with_workspace(dims, x, 1, 256)
+    got = without_allocation(dims, x, 1, 256)
+    for name, a, b in zip(("A_g", "Qp", "scores", "victims"), ref, got):
+        if a.dtype == torch.bfloat16:
+            a, b = a.view(torch.int16), b.view(torch.int16)
+        assert torch.equal(a, b), f"{name} differs after a failed call"
+
+
+def test_static_calls_back_to_back_with_different_batches():
+    # Static calls in a row, no workspace call between them: one sequence (the one-sequence
+    # ranking's part of the array), then 80 (the per-sequence counters), then one again.
+    dims = W.Dims(1, 32, 8, 128, 32, 16, 3000)
+    cases = [([2048], 256, 21), ([30] * 80, 16, 22), ([1500], 64, 23)]
+    got = []
+    for lengths, k, seed in cases:
+        x = inputs(dims, lengths, 1, 1, seed=seed)
+        got.append((x, k, without_allocation(dims, x, 0, k)))
+    for x, k, out in got:
+        ref = with_workspace(dims, x, 0, k)
+        for name, a, b in zip(("A_g", "Qp", "scores", "victims"), ref, out):
+            if a.dtype == torch.bfloat16:
+                a, b = a.view(torch.int16), b.view(torch.int16)
+            assert torch.equal(a, b), f"{x['S']} sequences: {name} differs"
