@@ -61,7 +61,8 @@ typedef enum hss_status {
     HSS_ERR_OUT_OF_RANGE = 2,        /* layer >= num_layers, or a block id outside [0, max_blocks) */
     HSS_ERR_NULL_POINTER = 3,        /* a required pointer is NULL */
     HSS_ERR_MISALIGNED = 4,          /* a bf16 tensor is not 16-byte aligned */
-    HSS_ERR_WORKSPACE_TOO_SMALL = 5, /* reserved for calls that take a workspace */
+    HSS_ERR_WORKSPACE_TOO_SMALL = 5, /* a caller workspace (hss_layer_step) or the static
+                                        array (hss_layer_step_static) is too small */
     HSS_ERR_UNSUPPORTED_SHAPE = 6,   /* valid dims that no kernel here handles */
     HSS_ERR_CUDA = 7,                /* a CUDA runtime call or a launch failed */
     HSS_ERR_DEVICE_TIMEOUT = 8,      /* a kernel gave up waiting on a pipeline barrier */
@@ -369,6 +370,26 @@ hss_status hss_layer_step_static(const hss_dims* dims, const uint16_t* P, const 
  * into the library's error word, and exits.  The context stays usable.
  */
 hss_status hss_self_test_wait_timeout(int32_t* dev_status, int64_t limit_ns, void* stream);
+
+/*
+ * Failure-detection self-test of hss_layer_step's one-sequence victim ranking.  In that
+ * ranking every CTA of the scorer waits until all of the sequence's keys are published, with
+ * a bounded wait.  This call runs the decode layer call's scorer on one sequence (one query
+ * row, queries projected in the scorer, no new blocks; the arguments as in hss_layer_step)
+ * with its last CTA withholding its keys, so that every CTA's wait runs out after limit_ns
+ * (1e3 .. 2e9) nanoseconds: HSS_ERR_DEVICE_TIMEOUT is stored into *dev_status and the
+ * library's error word, the kernel exits, the context stays usable.  The scores are
+ * written; the victims are not meaningful.  Zero the workspace again before the next
+ * hss_layer_step on it.  HSS_ERR_UNSUPPORTED_SHAPE (nothing launched) when the shape does not
+ * take that ranking (more than 4096 entries, or a grid that does not fit the GPU at once).
+ * No page has a counterpart: it tests this library's own wait.
+ */
+hss_status hss_self_test_spread_wait(const hss_dims* dims, const uint16_t* P, const uint16_t* Q,
+                                     uint16_t* A_g, int32_t layer, const int32_t* block_table,
+                                     const int32_t* seq_offsets, int64_t total_blocks,
+                                     float* scores, int32_t k, int32_t* victims, void* workspace,
+                                     size_t workspace_bytes, int64_t limit_ns,
+                                     int32_t* dev_status, void* stream);
 
 /*
  * Device-side error word of the current device: the first HSS_ERR_* code a

@@ -42,7 +42,7 @@ EXPORTED = (
     "hss_layer_step", "hss_layer_step_workspace_bytes", "hss_layer_step_static",
     "hss_score_blocks_masked",
     "hss_layer_step_static_max_seqs", "hss_write_kv_tokens", "hss_score_rows",
-    "hss_select_rows", "hss_self_test_wait_timeout",
+    "hss_select_rows", "hss_self_test_wait_timeout", "hss_self_test_spread_wait",
 )
 
 
@@ -114,6 +114,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                             i32, vp, vp]
     lib.hss_self_test_wait_timeout.restype = i32
     lib.hss_self_test_wait_timeout.argtypes = [vp, i64, vp]
+    lib.hss_self_test_spread_wait.restype = i32
+    lib.hss_self_test_spread_wait.argtypes = [dp, vp, vp, vp, i32, vp, vp, i64, vp, i32, vp, vp,
+                                              sz, i64, vp, vp]
     lib.hss_rank_victims.restype = i32
     lib.hss_rank_victims.argtypes = [vp, vp, i32, i64, i32, vp, vp]
     lib.hss_read_device_error.restype = i32
@@ -333,6 +336,21 @@ def hss_self_test_wait_timeout(dev_status, limit_ns: int, stream=None) -> None:
     """Launch a kernel whose bounded pipeline wait runs out (it sets dev_status)."""
     st = load().hss_self_test_wait_timeout(_ptr(dev_status), int(limit_ns), _stream(stream))
     _check(st, "hss_self_test_wait_timeout")
+
+
+def hss_self_test_spread_wait(dims, P, Q, A_g, layer: int, block_table, seq_offsets,
+                              total_blocks: int, scores, k: int, victims, workspace,
+                              workspace_bytes: int, limit_ns: int, dev_status=None,
+                              stream=None) -> None:
+    """Run the layer call's one-sequence ranking with one CTA withholding its keys, so that
+    the other CTAs' bounded waits run out after limit_ns (they set dev_status)."""
+    st = load().hss_self_test_spread_wait(ctypes.byref(hss_dims.of(dims)), _ptr(P), _ptr(Q),
+                                          _ptr(A_g), int(layer), _ptr(block_table),
+                                          _ptr(seq_offsets), int(total_blocks), _ptr(scores),
+                                          int(k), _ptr(victims), _ptr(workspace),
+                                          int(workspace_bytes), int(limit_ns), _ptr(dev_status),
+                                          _stream(stream))
+    _check(st, "hss_self_test_spread_wait")
 
 
 def hss_read_device_error(stream=None) -> int:

@@ -389,6 +389,31 @@ hss_status hss_layer_step(const hss_dims* dims, const uint16_t* P, const uint16_
     return HSS_OK;
 }
 
+hss_status hss_self_test_spread_wait(const hss_dims* dims, const uint16_t* P, const uint16_t* Q,
+                                     uint16_t* A_g, int32_t layer, const int32_t* block_table,
+                                     const int32_t* seq_offsets, int64_t total_blocks,
+                                     float* scores, int32_t k, int32_t* victims, void* workspace,
+                                     size_t workspace_bytes, int64_t limit_ns,
+                                     int32_t* dev_status, void* stream) {
+    if (limit_ns < 1000 || limit_ns > 2000000000) return HSS_ERR_INVALID_ARGUMENT;
+    LayerStepPlan plan;
+    hss_status st = layer_step_check(dims, P, nullptr, nullptr, 0, Q, 1, nullptr, A_g, layer,
+                                     block_table, seq_offsets, 1, total_blocks, scores, k,
+                                     victims, workspace, workspace_bytes, &plan);
+    if (st != HSS_OK) return st;
+    if (total_blocks == 0 || !plan.decode || !plan.inline_q) return HSS_ERR_UNSUPPORTED_SHAPE;
+    int32_t* ws = static_cast<int32_t*>(workspace);
+    FusedRank fr{ws + kSpreadRegionBytes / 4, ws, victims, k, false, nullptr, 0};
+    fr.wait_limit_ns = limit_ns;
+    fr.withhold_cta = 0x7FFFFFFF;  // past the grid: its last CTA
+    fr.require_spread = true;
+    ScoreArgs sa = plan.score;
+    sa.dev_status = dev_status;
+    const InlineQ iq{Q, P, dims->head_dim, false};
+    bool fused = false;
+    return launch_score_decode(sa, static_cast<cudaStream_t>(stream), &fr, &fused, &iq);
+}
+
 hss_status hss_score_rows(const hss_dims* dims, const uint16_t* Qp, int32_t rows,
                           const uint16_t* A_g, int32_t layer, const int32_t* block_table,
                           int64_t num_blocks, float* scores, int32_t* dev_status, void* stream) {

@@ -114,6 +114,12 @@ struct FusedRank {
     bool early;
     const int32_t* new_ids;
     int64_t num_new;
+    // Self-test of the one-sequence ranking's bounded wait: its limit (0: the library's), a CTA
+    // that withholds its keys (-1: none), and whether the call must take that ranking (else
+    // HSS_ERR_UNSUPPORTED_SHAPE, nothing launched).
+    int64_t wait_limit_ns = 0;
+    int32_t withhold_cta = -1;
+    bool require_spread = false;
 };
 // Queries projected inside the decode scorer (a.Qp unused): Q [num_seqs, rows, nq, hd] and
 // P [hd, r].  nowait: the kernel just before the scorer is this call's projection of the

@@ -99,6 +99,10 @@ struct DecodeParams {
     // mbarriers and of the eight slot buffers in shared memory.
     int32_t tma_bar_off;
     int32_t tma_buf_off;
+    // Spread ranking's wait on the other CTAs' words: its limit, and (self-test only, else -1)
+    // a CTA that withholds its words so that every other CTA's wait runs out.
+    uint64_t wait_limit_ns;
+    int32_t withhold_cta;
 };
 
 // TMA slot buffers: the largest slot and the most entries per warp they take.
@@ -715,7 +719,10 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
         }
         const uint32_t tag = *tag_smem;
         const int pos0 = static_cast<int>(eb - a);  // position of this CTA's first entry
-        if (static_cast<int>(threadIdx.x) < cnt)
+        // (self-test: the withheld CTA, an index past the grid meaning its last one)
+        const int withheld = p.withhold_cta < 0 ? -1
+                             : min(p.withhold_cta, static_cast<int>(gridDim.x) - 1);
+        if (static_cast<int>(threadIdx.x) < cnt && static_cast<int>(blockIdx.x) != withheld)
             st_relaxed_gpu_u64(&words[pos0 + threadIdx.x],
                                (static_cast<uint64_t>(tag) << 32) | ekey[eb - cb + threadIdx.x]);
         // Gather: 16 words per thread (slot q holds position tid + 256 q); slots past the
@@ -744,7 +751,7 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
                     missing &= ~(1u << q);
                 }
             }
-            if (missing != 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+            if (missing != 0 && global_timer_ns() - t0 > p.wait_limit_ns) {
                 raise_error(p.dev_status, p.lib_error, HSS_ERR_DEVICE_TIMEOUT);
                 break;
             }
@@ -967,6 +974,9 @@ hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream, const Fu
     p.nowait = 0;
     p.tma_bar_off = 0;
     p.tma_buf_off = 0;
+    p.wait_limit_ns = fr != nullptr && fr->wait_limit_ns > 0
+                          ? static_cast<uint64_t>(fr->wait_limit_ns) : kWaitLimitNs;
+    p.withhold_cta = fr != nullptr ? fr->withhold_cta : -1;
     if (fr != nullptr && fr->early && fr->num_new <= 64) {
         p.new_ids = fr->new_ids;
         p.num_new = static_cast<int32_t>(fr->num_new);
@@ -1042,6 +1052,7 @@ hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream, const Fu
             if (fused != nullptr) *fused = true;
         }
     }
+    if (fr != nullptr && fr->require_spread && !p.spread) return HSS_ERR_UNSUPPORTED_SHAPE;
     if (!p.spread && fr != nullptr && fr->counters != nullptr && warps_per_cta == kWarpsMax &&
         a.total <= kWarpsMax * 32 * rankdev::keys_per_thread<kWarpsMax * 32>()) {
         const int sel_cap = rankdev::rank_sel_cap(fr->k);
