@@ -210,6 +210,65 @@ __device__ __forceinline__ void tmem_ld_wait() {
 
 // 32 TMEM lanes x 16 consecutive 32-bit columns: thread i of the warp receives lane
 // (warp's lane quarter base + i), columns [col, col + 16).
+// Max over the N fp32 columns [taddr, taddr + N) of this thread's TMEM lane (N = 4, 8, 16 or
+// 32), taken in the TMEM load path itself (tcgen05.ld.red, sm_103a): NaN-ignoring like
+// fmaxf, +0 above -0, -inf when every column is -inf (checked on a GB300 against a plain
+// max).  The instruction also returns an N-register vector, which these helpers drop.  The
+// value may be used only after the wait (tmem_ld_wait_values, or tmem_ld_wait followed by
+// order_after_wait on it).
+template <int N>
+__device__ __forceinline__ float tmem_ldred_max(uint32_t taddr);
+
+template <>
+__device__ __forceinline__ float tmem_ldred_max<4>(uint32_t taddr) {
+    uint32_t v[4];
+    float m;
+    asm volatile("tcgen05.ld.red.sync.aligned.32x32b.x4.max.f32 {%0,%1,%2,%3}, %4, [%5];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=f"(m)
+                 : "r"(taddr));
+    return m;
+}
+template <>
+__device__ __forceinline__ float tmem_ldred_max<8>(uint32_t taddr) {
+    uint32_t v[8];
+    float m;
+    asm volatile("tcgen05.ld.red.sync.aligned.32x32b.x8.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, %8, [%9];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=f"(m)
+                 : "r"(taddr));
+    return m;
+}
+template <>
+__device__ __forceinline__ float tmem_ldred_max<16>(uint32_t taddr) {
+    uint32_t v[16];
+    float m;
+    asm volatile("tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, %16, [%17];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=f"(m)
+                 : "r"(taddr));
+    return m;
+}
+template <>
+__device__ __forceinline__ float tmem_ldred_max<32>(uint32_t taddr) {
+    uint32_t v[32];
+    float m;
+    asm volatile("tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31]), "=f"(m)
+                 : "r"(taddr));
+    return m;
+}
+
+__device__ __forceinline__ float tmem_ldred_max_x32(uint32_t taddr) {
+    return tmem_ldred_max<32>(taddr);
+}
+
+// After a tcgen05.wait::ld: makes a value loaded before the wait count as produced after it,
+// so its uses cannot be scheduled ahead of the wait.
+__device__ __forceinline__ void order_after_wait(float& x) { asm volatile("" : "+f"(x)::"memory"); }
+
+// tcgen05.wait::ld that also orders the use of four values loaded before it.
+__device__ __forceinline__ void tmem_ld_wait_values(float& a, float& b, float& c, float& d) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+f"(a), "+f"(b), "+f"(c), "+f"(d)::"memory");
+}
+
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t* v) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "

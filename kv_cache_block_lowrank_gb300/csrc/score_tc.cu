@@ -514,7 +514,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // row maxima at once; the accumulator is released before the shuffles.
                     constexpr int V = 128 / ROWG;
                     float xr[V];
-                    if (valid > 0) {
+                    if (valid == 128) {
+                        // Every column real: each row's max over its g heads (g consecutive
+                        // columns) is taken in the TMEM load path, one reduction per row.
+#pragma unroll
+                        for (int i = 0; i < V; ++i)
+                            xr[i] = tmem_ldred_max<ROWG>(taddr + static_cast<uint32_t>(i * ROWG));
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < V; ++i) order_after_wait(xr[i]);
+                    } else if (valid > 0) {
                         uint32_t va[64];
                         tmem_ld_32x32b_x32(taddr, va);
                         tmem_ld_32x32b_x32(taddr + 32, va + 32);
@@ -585,6 +594,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     continue;
+                } else if (!MASKED && valid == 128) {
+                    // Every column a real query vector: the max over them is taken in the
+                    // TMEM load path (four 32-column reductions), no register copy to scan.
+                    any = true;
+                    float m0 = tmem_ldred_max_x32(taddr);
+                    float m1 = tmem_ldred_max_x32(taddr + 32);
+                    float m2 = tmem_ldred_max_x32(taddr + 64);
+                    float m3 = tmem_ldred_max_x32(taddr + 96);
+                    tmem_ld_wait_values(m0, m1, m2, m3);
+                    run = fmax3(run, fmaxf(m0, m1), fmaxf(m2, m3));
                 } else if (valid > 0) {
                     any = true;
                     uint32_t v[128];
