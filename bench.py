@@ -193,14 +193,14 @@ def measured_peaks():
 # dram__bytes_write.sum) from the ncu captures summarised in profiles/, or None when the
 # kernel has changed since its capture.
 TRAFFIC = {
-    "decode": None,  # the layer-step kernel changed since its last capture
+    "decode": (16882432 + 0, "profiles/score_decode_layer_step.md"),
     "batched": (283580928 + 2741504, "profiles/score_decode_batched.md"),
-    "prefill": None,  # the kernel's epilogue changed since its last capture
+    "prefill": (143540224, "profiles/score_tc_prefill.md"),
     # captured on a 40000-block launch; traffic grows with the blocks, so scaled to 4096
     "ingest": (round((1310970000 + 305094400) * 4096 / 40000),
                "profiles/project_ingest_40000_blocks.md, scaled from 40000 to 4096 blocks"),
     "ingest_tokens": (134817280 + 112388096, "profiles/project_tokens_65536.md"),
-    "prefill_rows": None,  # the kernel's epilogue changed since its last capture
+    "prefill_rows": (160649472, "profiles/score_tc_prefill_rows.md"),
 }
 
 

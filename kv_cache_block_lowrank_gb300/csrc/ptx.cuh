@@ -219,6 +219,9 @@ __device__ __forceinline__ void tmem_ld_wait() {
 template <int N>
 __device__ __forceinline__ float tmem_ldred_max(uint32_t taddr);
 
+// (the vector the instruction also writes is dropped on purpose)
+#pragma nv_diag_suppress 550
+
 template <>
 __device__ __forceinline__ float tmem_ldred_max<4>(uint32_t taddr) {
     uint32_t v[4];
@@ -255,6 +258,8 @@ __device__ __forceinline__ float tmem_ldred_max<32>(uint32_t taddr) {
                  : "r"(taddr));
     return m;
 }
+
+#pragma nv_diag_default 550
 
 __device__ __forceinline__ float tmem_ldred_max_x32(uint32_t taddr) {
     return tmem_ldred_max<32>(taddr);
