@@ -271,11 +271,11 @@ hss_status hss_select_rows(const float* scores, int32_t rows, int64_t num_blocks
  *   hss_rank_victims
  * on the same stream (the same kernels compute them; the victims are the same words in
  * the same order).  In the decode regime the victim ranking runs inside the scoring kernel:
- * for one sequence of at most 4096 blocks whose scoring grid fits on the GPU at once, every
- * CTA publishes its blocks' keys in the workspace, waits until the sequence's keys are all
- * there (a bounded wait: HSS_ERR_DEVICE_TIMEOUT after 1 s) and places its own blocks by
- * counting the smaller (score, position) words; otherwise the last CTA to finish a sequence
- * ranks it.  That bounded wait assumes the scoring grid gets the whole GPU: a kernel of
+ * for at most 8 sequences and 4096 blocks in all, when the scoring grid fits on the GPU at
+ * once, every CTA publishes its blocks' keys in the workspace, waits until all the call's
+ * keys are there (a bounded wait: HSS_ERR_DEVICE_TIMEOUT after 1 s) and places its own blocks
+ * by counting the smaller (sequence, score, position) words; otherwise the last CTA to finish
+ * a sequence ranks it.  That bounded wait assumes the scoring grid gets the whole GPU: a kernel of
  * another stream that holds SMs for longer than the limit makes the call report
  * HSS_ERR_DEVICE_TIMEOUT (its victims are then wrong; zero the workspace before the next call).
  * This is the fused decode call the predictor page's per-step usage implies (module docs

@@ -117,6 +117,10 @@ constexpr int kSpreadMaxCta = 16;
 // Its workspace region (p.counters in spread mode): the call number (a line of its own), then
 // from byte 256 one tagged word per entry (32 KiB).
 constexpr int kSpreadWordsOffsetWords = 64;
+// ... at most this many sequences (their index takes 3 bits of a word), and the call number's
+// bits kept in a word (above the sequence and the 32-bit key).
+constexpr int kSpreadMaxSeqs = 8;
+constexpr uint32_t kSpreadTagMask = (1u << 29) - 1u;
 
 // below -= [w < we] for 64-bit unsigned words: one borrow chain, no predicate or branch (a
 // compare-and-select per pair issued about twice the instructions).
@@ -682,38 +686,52 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
     if (p.counters == nullptr) return;
 
     if (p.spread) {
-        // ---- spread ranking of the one sequence [a, b): the rank of entry e is the number
-        // of words (key << 32 | position) below its own; entry e is victim number rank(e)
-        // when that is below k.  The words are unique, so the ranks are a permutation.
+        // ---- spread ranking of the call's S <= 8 sequences, at most 4096 entries in all.
         // Every CTA publishes its entries' keys in the workspace as 64-bit words tagged with
-        // this call's number (tag << 32 | key, one relaxed store each) and reads the
-        // sequence's words until every one carries the tag: each word is its own
+        // this call's number (tag << 35 | sequence << 32 | key, one relaxed store each) and
+        // reads all the call's words until every one carries the tag: each word is its own
         // completion flag, so no counter, fence or second read of the scores is needed.
+        // The rank of entry e of sequence s is then the number of counting words
+        // (sequence << 44 | key << 12 | position) below its own, less the entries of the
+        // sequences before s (their words all lie below); entry e is victim number rank(e)
+        // of its sequence when that is below k.  The words are unique, so within a sequence
+        // the ranks are a permutation, ordered by (key, position).
         uint32_t* ekey = reinterpret_cast<uint32_t*>(smem_dec + p.frag_bytes_cta);
         uint32_t* part = ekey + p.todo_cap;  // [warp][kSpreadMaxCta] partial counts, then
-        uint32_t* tag_smem = part + kWarpsMax * kSpreadMaxCta;  // this call's tag
+        uint32_t* tag_smem = part + kWarpsMax * kSpreadMaxCta;  // this call's tag,
+        int32_t* soff = reinterpret_cast<int32_t*>(tag_smem + 4);  // seq_offsets[0 .. S],
+        uint8_t* eseq = reinterpret_cast<uint8_t*>(soff + kSpreadMaxSeqs + 1);  // entries' seqs
+        const int S = p.num_seqs;
         const int64_t per_cta = p.entries_per_warp * (blockDim.x >> 5);
         const int64_t cb = static_cast<int64_t>(blockIdx.x) * per_cta;
-        // (loaded before the barrier: the latency overlaps the CTA's slowest warp)
-        const int64_t a = __ldg(&p.seq_offsets[0]), b = __ldg(&p.seq_offsets[1]);
-        const int64_t eb = max(cb, a), ee = min(min(p.total, cb + per_cta), b);
-        const int cnt = ee > eb ? static_cast<int>(ee - eb) : 0;  // <= kSpreadMaxCta
-        if (a < 0 || b < a || min(b, p.total) - a > kSpreadMaxEntries) {
-            // Offsets that do not describe one sequence of at most 4096 of the scored
-            // entries: nothing is published (the keys region holds 4096 words).
+        int* epoch = p.counters;
+        uint64_t* words = reinterpret_cast<uint64_t*>(p.counters + kSpreadWordsOffsetWords);
+        if (static_cast<int>(threadIdx.x) <= S) soff[threadIdx.x] = __ldg(&p.seq_offsets[threadIdx.x]);
+        if (threadIdx.x == 0)
+            *tag_smem = (static_cast<uint32_t>(ld_relaxed_gpu(epoch)) + 1u) & kSpreadTagMask;
+        __syncthreads();  // this CTA's keys, the tag and the offsets
+        const int64_t a = soff[0], b = soff[S];
+        if (a < 0 || b < a || b > p.total || b - a > kSpreadMaxEntries) {
+            // Offsets that do not describe at most 4096 of the scored entries: nothing is
+            // published (the keys region holds 4096 words).
             if (threadIdx.x == 0) raise_error(p.dev_status, p.lib_error, HSS_ERR_OUT_OF_RANGE);
             grid_launch_dependents();
             return;
         }
-        const int n = static_cast<int>(min(b, p.total) - a);
-        int* epoch = p.counters;
-        uint64_t* words = reinterpret_cast<uint64_t*>(p.counters + kSpreadWordsOffsetWords);
-        if (threadIdx.x == 0) *tag_smem = static_cast<uint32_t>(ld_relaxed_gpu(epoch)) + 1u;
-        __syncthreads();  // this CTA's keys and the tag
-        if (cnt == 0) {  // no entry of the sequence in this CTA
-            if (blockIdx.x == 0)
-                for (int j = max(n, 0) + static_cast<int>(threadIdx.x); j < p.k; j += blockDim.x)
-                    p.victims[j] = -1;
+        const int n = static_cast<int>(b - a);
+        const int64_t eb = max(cb, a), ee = min(min(p.total, cb + per_cta), b);
+        const int cnt = ee > eb ? static_cast<int>(ee - eb) : 0;  // <= kSpreadMaxCta
+        // Sequences with fewer entries than k end their rows with -1 (CTA 0 writes them).
+        auto pad_rows = [&]() {
+            if (blockIdx.x != 0) return;
+            for (int q = 0; q < S; ++q) {
+                const int nq = soff[q + 1] - soff[q];
+                for (int j = max(nq, 0) + static_cast<int>(threadIdx.x); j < p.k; j += blockDim.x)
+                    p.victims[static_cast<int64_t>(q) * p.k + j] = -1;
+            }
+        };
+        if (cnt == 0) {  // no entry of the call in this CTA
+            pad_rows();
             grid_launch_dependents();
             return;
         }
@@ -722,11 +740,18 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
         // (self-test: the withheld CTA, an index past the grid meaning its last one)
         const int withheld = p.withhold_cta < 0 ? -1
                              : min(p.withhold_cta, static_cast<int>(gridDim.x) - 1);
-        if (static_cast<int>(threadIdx.x) < cnt && static_cast<int>(blockIdx.x) != withheld)
-            st_relaxed_gpu_u64(&words[pos0 + threadIdx.x],
-                               (static_cast<uint64_t>(tag) << 32) | ekey[eb - cb + threadIdx.x]);
+        if (static_cast<int>(threadIdx.x) < cnt) {
+            const int64_t i = eb + threadIdx.x;
+            int se = 0;  // this entry's sequence
+            while (se + 1 < S && soff[se + 1] <= i) ++se;
+            eseq[threadIdx.x] = static_cast<uint8_t>(se);
+            if (static_cast<int>(blockIdx.x) != withheld)
+                st_relaxed_gpu_u64(&words[pos0 + threadIdx.x],
+                                   (static_cast<uint64_t>(tag) << 35) |
+                                       (static_cast<uint64_t>(se) << 32) | ekey[eb - cb + threadIdx.x]);
+        }
         // Gather: 16 words per thread (slot q holds position tid + 256 q); slots past the
-        // end hold a word above every real one (NaN and +inf map to key 0xFF800000).
+        // end hold a word above every real one.
         uint64_t w[kSpreadKeysPerThread];
         uint32_t missing = 0;
 #pragma unroll
@@ -746,8 +771,9 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
 #pragma unroll
             for (int q = 0; q < kSpreadKeysPerThread; ++q) {
                 const int j = static_cast<int>(threadIdx.x) + q * kWarpsMax * 32;
-                if (((missing >> q) & 1u) && static_cast<uint32_t>(v[q] >> 32) == tag) {
-                    w[q] = (v[q] << 32) | static_cast<uint32_t>(j);
+                if (((missing >> q) & 1u) && static_cast<uint32_t>(v[q] >> 35) == tag) {
+                    w[q] = (((v[q] >> 32) & 7ull) << 44) | ((v[q] & 0xFFFFFFFFull) << 12) |
+                           static_cast<uint32_t>(j);
                     missing &= ~(1u << q);
                 }
             }
@@ -756,22 +782,23 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
                 break;
             }
         }
-        __syncthreads();  // every thread of this CTA has seen every word
+        __syncthreads();  // every thread of this CTA has seen every word (and eseq is set)
         grid_launch_dependents();
-        // Every CTA has published, so every CTA has read the tag: the sequence's first CTA
-        // advances the call number for the next call.
+        // Every CTA has published, so every CTA has read the tag: the CTA holding the call's
+        // first entry advances the call number for the next call.
         if (threadIdx.x == 0 && static_cast<int64_t>(blockIdx.x) == a / per_cta)
             st_relaxed_gpu_s32(epoch, static_cast<int>(tag));
         // Four entries at a time; each warp leaves its four totals in `part`, lane u writing
-        // entry e0 + u (no atomics, no branch per entry).  Slots past the sequence hold a word
-        // above every real one, so half the slots are skipped whole when n <= 2048.
+        // entry e0 + u (no atomics, no branch per entry).  Slots past the call's entries hold
+        // a word above every real one, so half the slots are skipped whole when n <= 2048.
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
         for (int e0 = 0; e0 < cnt; e0 += 4) {
             uint64_t we[4];
             uint32_t neg[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                we[u] = e0 + u < cnt ? (static_cast<uint64_t>(ekey[eb - cb + e0 + u]) << 32) |
+                we[u] = e0 + u < cnt ? (static_cast<uint64_t>(eseq[e0 + u]) << 44) |
+                                           (static_cast<uint64_t>(ekey[eb - cb + e0 + u]) << 12) |
                                            static_cast<uint32_t>(pos0 + e0 + u)
                                      : 0ull;
                 neg[u] = 0;
@@ -789,15 +816,17 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
         }
         __syncthreads();
         if (static_cast<int>(threadIdx.x) < cnt) {
-            uint32_t rank = 0;
+            const int se = eseq[threadIdx.x];
+            uint32_t below = 0;
 #pragma unroll
-            for (int wv = 0; wv < kWarpsMax; ++wv) rank += part[wv * kSpreadMaxCta + threadIdx.x];
+            for (int wv = 0; wv < kWarpsMax; ++wv) below += part[wv * kSpreadMaxCta + threadIdx.x];
+            const int64_t first = soff[se];  // the words of earlier sequences all lie below
+            const uint32_t rank = below - static_cast<uint32_t>(first - a);
             if (rank < static_cast<uint32_t>(p.k))
-                p.victims[rank] = pos0 + static_cast<int>(threadIdx.x);
+                p.victims[static_cast<int64_t>(se) * p.k + rank] =
+                    static_cast<int32_t>(eb + threadIdx.x - first);
         }
-        if (blockIdx.x == 0)
-            for (int j = n + static_cast<int>(threadIdx.x); j < p.k; j += blockDim.x)
-                p.victims[j] = -1;
+        pad_rows();
         return;
     }
 
@@ -1024,12 +1053,14 @@ hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream, const Fu
     const int nt = (p.nvec + 7) / 8;
     p.spread = 0;
     if (fr != nullptr && fr->spread_region != nullptr && warps_per_cta == kWarpsMax &&
-        a.num_seqs == 1 && a.total <= kSpreadMaxEntries &&
+        a.num_seqs >= 1 && a.num_seqs <= kSpreadMaxSeqs && a.total <= kSpreadMaxEntries &&
         (reinterpret_cast<uintptr_t>(fr->spread_region) & 7u) == 0 &&
         p.entries_per_warp * warps_per_cta <= kSpreadMaxCta) {
         // Spread ranking needs the whole grid resident at once (its CTAs wait for each other).
         const int todo_cap = static_cast<int>(p.entries_per_warp * warps_per_cta);
-        const int smem_spread = smem + 4 * todo_cap + 4 * kWarpsMax * kSpreadMaxCta + 16;
+        // ... then the call tag, the sequence offsets and the entries' sequence indices.
+        const int smem_spread = smem + 4 * todo_cap + 4 * kWarpsMax * kSpreadMaxCta + 16 +
+                                4 * (kSpreadMaxSeqs + 1) + kSpreadMaxCta + 12;
         int per_sm = 0;
 #define HSS_DECODE_CASE(KS, NT_) \
     if (ksteps == KS && nt == NT_) per_sm = ctas_per_sm_t<KS, NT_>(p, smem_spread);

@@ -375,3 +375,46 @@ def test_prepared_layer_step_equals_the_plain_call(inline):
     assert torch.equal(out[0][0].view(torch.int16), out[1][0].view(torch.int16))
     assert torch.equal(out[0][1], out[1][1])
     assert torch.equal(out[0][2], out[1][2])
+
+
+# Up to 8 sequences and 4096 entries in all: the scorer's CTAs rank every sequence together
+# (one word per entry, sequence index inside the word).  Victims must equal the ranking
+# kernel's bit for bit, over three calls on one workspace.
+@pytest.mark.parametrize("lengths,k,ties,inline", [
+    ([1024, 1024], 256, 0, True),                       # two halves of the decode layer
+    ([500, 0, 1300, 7], 64, 0, True),                   # an empty sequence, one shorter than k
+    ([600] * 6 + [300, 96], 128, 0, False),             # eight sequences, Qp given
+    ([2000, 2000, 96], 300, 0, True),                   # 4096 entries in all (the limit)
+    ([2000, 2097], 64, 0, True),                        # 4097: the last CTA ranks instead
+    ([700, 700, 700], 700, 13, True),                   # k == n, many equal scores
+    ([1, 1, 1, 1, 1], 8, 0, True),                      # five one-block sequences
+])
+def test_layer_step_few_sequences_ranking(lengths, k, ties, inline):
+    d = W.Dims(1, 32, 8, 128, 32, 16, 6000)
+    x = make(d, lengths, 1, 1, seed=sum(lengths) + k + ties)
+    if ties:
+        x = _with_ties(x, d, ties, seed=k)
+    S, n = len(lengths), sum(lengths)
+    _, _, sc1, vic1 = separate(d, x, 0, k)
+    A = x["A"].clone()
+    sc = torch.empty(n, dtype=torch.float32, device=DEV)
+    vic = torch.full((S, k), 12345, dtype=torch.int32, device=DEV)
+    nb = hss.hss_layer_step_workspace_bytes(S)
+    ws = torch.zeros(max(nb, 4) // 4, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    Qp = None if inline else torch.empty(S, 1, d.num_q_heads, d.r, dtype=torch.bfloat16,
+                                         device=DEV)
+    for _ in range(3):
+        vic.fill_(12345)
+        hss.hss_layer_step(d, x["P"], x["K_new"], x["new_ids"], x["n_new"], x["Q"], 1, Qp, A, 0,
+                           x["table"], x["offs"], S, n, sc, k, vic, ws, nb, st)
+        ref = torch.empty(S, k, dtype=torch.int32, device=DEV)
+        hss.hss_rank_victims(sc, x["offs"], S, n, k, ref)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert counters_zero(ws, S), "the counters must be left zeroed"
+        assert torch.equal(vic, ref)
+        if inline:
+            assert torch.allclose(sc, sc1, rtol=2e-3, atol=1e-2)
+        else:
+            assert torch.equal(sc, sc1) and torch.equal(vic, vic1)
