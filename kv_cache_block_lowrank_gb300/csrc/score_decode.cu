@@ -136,17 +136,6 @@ __device__ __forceinline__ void sub_if_less(uint32_t& below, uint64_t w, uint64_
           "r"(static_cast<uint32_t>(we)), "r"(static_cast<uint32_t>(we >> 32)));
 }
 
-// neg_below[u] -= the number of the first SLOTS words w[] below we[u].  The slot count is a
-// template parameter: a per-slot test inside the unrolled loop cost as much as the compares.
-template <int SLOTS, int N>
-__device__ __forceinline__ void count_below(const uint64_t (&w)[N], const uint64_t (&we)[4],
-                                            uint32_t (&neg_below)[4]) {
-#pragma unroll
-    for (int q = 0; q < SLOTS; ++q)
-#pragma unroll
-        for (int u = 0; u < 4; ++u) sub_if_less(neg_below[u], w[q], we[u]);
-}
-
 __device__ __forceinline__ int ld_relaxed_gpu(const int* addr) {
     int v;
     asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
@@ -165,6 +154,107 @@ __device__ __forceinline__ void st_relaxed_gpu_u64(uint64_t* addr, uint64_t v) {
 
 __device__ __forceinline__ void st_relaxed_gpu_s32(int* addr, int v) {
     asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
+// Totals over the warp of eight per-lane counts: afterwards lane l holds the total of
+// c[(l >> 2) & 7].  Three exchanges each halve the counts a lane carries (it keeps the half
+// its lane bit selects and adds its partner's copy of that half), then two plain ones finish
+// the sums: nine shuffles for eight totals.
+__device__ __forceinline__ uint32_t warp_sum8(const uint32_t (&c)[8]) {
+    const int lane = static_cast<int>(threadIdx.x) & 31;
+    const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0, b2 = (lane & 4) != 0;
+    uint32_t a[4], h[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        a[i] = (b4 ? c[i + 4] : c[i]) + __shfl_xor_sync(0xffffffffu, b4 ? c[i] : c[i + 4], 16);
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        h[i] = (b3 ? a[i + 2] : a[i]) + __shfl_xor_sync(0xffffffffu, b3 ? a[i] : a[i + 2], 8);
+    uint32_t x = (b2 ? h[1] : h[0]) + __shfl_xor_sync(0xffffffffu, b2 ? h[0] : h[1], 4);
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    return x;
+}
+
+// Spread ranking's gather: polls the call's n published words (slot q of thread t holds
+// position t + 256 q) until each carries the tag, and in every round counts the words that
+// arrived in it below each of the CTA's entries' counting words: neg[u] -= that count.  A
+// slot in which no lane of the warp saw a word arrive is skipped, so the counting mostly
+// overlaps the wait for the last CTA's words.  Returns false when the wait ran out.
+template <int SLOTS, int E>
+__device__ __forceinline__ bool spread_gather_count(const uint64_t* words, int n, uint32_t tag,
+                                                    const uint64_t (&we)[E], uint32_t (&neg)[E],
+                                                    uint64_t limit_ns) {
+    uint32_t missing = 0;
+#pragma unroll
+    for (int q = 0; q < SLOTS; ++q)
+        if (static_cast<int>(threadIdx.x) + q * kWarpsMax * 32 < n) missing |= 1u << q;
+    const uint64_t t0 = global_timer_ns();
+    while (__any_sync(0xffffffffu, missing != 0)) {
+        uint64_t v[SLOTS];
+#pragma unroll
+        for (int q = 0; q < SLOTS; ++q) {
+            const int j = static_cast<int>(threadIdx.x) + q * kWarpsMax * 32;
+            v[q] = (missing >> q) & 1u ? ld_relaxed_gpu_u64(&words[j]) : 0ull;
+        }
+        uint32_t arrived = 0;
+#pragma unroll
+        for (int q = 0; q < SLOTS; ++q) {
+            const int j = static_cast<int>(threadIdx.x) + q * kWarpsMax * 32;
+            const bool now = ((missing >> q) & 1u) && static_cast<uint32_t>(v[q] >> 35) == tag;
+            arrived |= static_cast<uint32_t>(now) << q;
+            // the counting word: sequence << 44 | key << 12 | position
+            v[q] = now ? (((v[q] >> 32) & 7ull) << 44) | ((v[q] & 0xFFFFFFFFull) << 12) |
+                             static_cast<uint32_t>(j)
+                       : ~0ull;
+        }
+        missing &= ~arrived;
+#pragma unroll
+        for (int q = 0; q < SLOTS; ++q)
+            if (__any_sync(0xffffffffu, (arrived >> q) & 1u))
+#pragma unroll
+                for (int u = 0; u < E; ++u) sub_if_less(neg[u], v[q], we[u]);
+        if (__any_sync(0xffffffffu, missing != 0 && global_timer_ns() - t0 > limit_ns))
+            return false;
+    }
+    return true;
+}
+
+// The CTA's cnt <= E entries (positions pos0 .. pos0 + cnt - 1 of the call, keys keys[],
+// sequences from the S + 1 offsets soff relative to the call's first entry eb - pos0): gathers
+// every word, counts those below each entry's word and leaves this warp's count of entry e in
+// part_warp[e].  Returns false when the wait ran out.
+template <int E>
+__device__ __forceinline__ bool spread_count(const uint64_t* words, int n, uint32_t tag,
+                                             uint64_t limit_ns, const int32_t* soff, int S,
+                                             const uint32_t* keys, int64_t eb, int pos0,
+                                             int cnt, uint32_t* part_warp) {
+    uint64_t we[E];
+    uint32_t neg[E];
+#pragma unroll
+    for (int u = 0; u < E; ++u) {
+        int se = 0;  // entry u's sequence
+        for (int t = 1; t < S; ++t) se += static_cast<int64_t>(soff[t]) <= eb + u;
+        we[u] = u < cnt ? (static_cast<uint64_t>(se) << 44) |
+                              (static_cast<uint64_t>(keys[u]) << 12) |
+                              static_cast<uint32_t>(pos0 + u)
+                        : 0ull;  // no word lies below it
+        neg[u] = 0;
+    }
+    const bool ok = n <= 8 * kWarpsMax * 32
+                        ? spread_gather_count<8, E>(words, n, tag, we, neg, limit_ns)
+                        : spread_gather_count<16, E>(words, n, tag, we, neg, limit_ns);
+    const int lane = static_cast<int>(threadIdx.x) & 31;
+#pragma unroll
+    for (int g = 0; g < E / 8; ++g) {
+        uint32_t c[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c[i] = neg[8 * g + i];
+        const uint32_t tot = 0u - warp_sum8(c);
+        const int e = 8 * g + ((lane >> 2) & 7);
+        if ((lane & 3) == 0 && e < cnt) part_warp[e] = tot;
+    }
+    return ok;
 }
 
 __device__ __forceinline__ int atom_add_acq_rel_gpu(int* addr, int v) {
@@ -750,71 +840,20 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
                                    (static_cast<uint64_t>(tag) << 35) |
                                        (static_cast<uint64_t>(se) << 32) | ekey[eb - cb + threadIdx.x]);
         }
-        // Gather: 16 words per thread (slot q holds position tid + 256 q); slots past the
-        // end hold a word above every real one.
-        uint64_t w[kSpreadKeysPerThread];
-        uint32_t missing = 0;
-#pragma unroll
-        for (int q = 0; q < kSpreadKeysPerThread; ++q) {
-            const int j = static_cast<int>(threadIdx.x) + q * kWarpsMax * 32;
-            w[q] = ~0ull;
-            if (j < n) missing |= 1u << q;
-        }
-        const uint64_t t0 = global_timer_ns();
-        while (missing != 0) {
-            uint64_t v[kSpreadKeysPerThread];
-#pragma unroll
-            for (int q = 0; q < kSpreadKeysPerThread; ++q) {
-                const int j = static_cast<int>(threadIdx.x) + q * kWarpsMax * 32;
-                v[q] = (missing >> q) & 1u ? ld_relaxed_gpu_u64(&words[j]) : 0ull;
-            }
-#pragma unroll
-            for (int q = 0; q < kSpreadKeysPerThread; ++q) {
-                const int j = static_cast<int>(threadIdx.x) + q * kWarpsMax * 32;
-                if (((missing >> q) & 1u) && static_cast<uint32_t>(v[q] >> 35) == tag) {
-                    w[q] = (((v[q] >> 32) & 7ull) << 44) | ((v[q] & 0xFFFFFFFFull) << 12) |
-                           static_cast<uint32_t>(j);
-                    missing &= ~(1u << q);
-                }
-            }
-            if (missing != 0 && global_timer_ns() - t0 > p.wait_limit_ns) {
-                raise_error(p.dev_status, p.lib_error, HSS_ERR_DEVICE_TIMEOUT);
-                break;
-            }
-        }
-        __syncthreads();  // every thread of this CTA has seen every word (and eseq is set)
+        // Gather every word, counting as they arrive; each warp leaves its count of each of
+        // the CTA's entries in `part` (no atomics).
+        const bool ok = cnt <= 8
+            ? spread_count<8>(words, n, tag, p.wait_limit_ns, soff, S, ekey + (eb - cb), eb,
+                              pos0, cnt, part + warp * kSpreadMaxCta)
+            : spread_count<16>(words, n, tag, p.wait_limit_ns, soff, S, ekey + (eb - cb), eb,
+                               pos0, cnt, part + warp * kSpreadMaxCta);
+        if (!ok && lane == 0) raise_error(p.dev_status, p.lib_error, HSS_ERR_DEVICE_TIMEOUT);
+        __syncthreads();  // every thread has seen every word; the counts and eseq are set
         grid_launch_dependents();
         // Every CTA has published, so every CTA has read the tag: the CTA holding the call's
         // first entry advances the call number for the next call.
         if (threadIdx.x == 0 && static_cast<int64_t>(blockIdx.x) == a / per_cta)
             st_relaxed_gpu_s32(epoch, static_cast<int>(tag));
-        // Four entries at a time; each warp leaves its four totals in `part`, lane u writing
-        // entry e0 + u (no atomics, no branch per entry).  Slots past the call's entries hold
-        // a word above every real one, so half the slots are skipped whole when n <= 2048.
-        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        for (int e0 = 0; e0 < cnt; e0 += 4) {
-            uint64_t we[4];
-            uint32_t neg[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                we[u] = e0 + u < cnt ? (static_cast<uint64_t>(eseq[e0 + u]) << 44) |
-                                           (static_cast<uint64_t>(ekey[eb - cb + e0 + u]) << 12) |
-                                           static_cast<uint32_t>(pos0 + e0 + u)
-                                     : 0ull;
-                neg[u] = 0;
-            }
-            if (n <= kSpreadKeysPerThread / 2 * kWarpsMax * 32)
-                count_below<kSpreadKeysPerThread / 2>(w, we, neg);
-            else
-                count_below<kSpreadKeysPerThread>(w, we, neg);
-            uint32_t tot[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) tot[u] = __reduce_add_sync(0xffffffffu, 0u - neg[u]);
-            const uint32_t mine = lane == 0 ? tot[0] : lane == 1 ? tot[1] : lane == 2 ? tot[2]
-                                                                               : tot[3];
-            if (lane < 4 && e0 + lane < cnt) part[warp * kSpreadMaxCta + e0 + lane] = mine;
-        }
-        __syncthreads();
         if (static_cast<int>(threadIdx.x) < cnt) {
             const int se = eseq[threadIdx.x];
             uint32_t below = 0;

@@ -216,6 +216,28 @@ def test_layer_step_several_new_blocks(first, n_new):
     inline_vs_oracle(d, x, 1, 256)
 
 
+def test_layer_step_new_block_named_twice():
+    # One new block at two table positions far apart (scored by different CTAs, each of which
+    # projects it) and a second new block at the next position: every copy scores alike.
+    d = W.Dims(2, 32, 8, 128, 32, 16, 2100)
+    x = make(d, [2048], 1, 2, seed=77)
+    x["table"][1500] = x["table"][3]
+    x["new_ids"] = x["table"][3:5].contiguous()
+    A, sc, _ = inline_vs_oracle(d, x, 1, 256)
+    assert float(sc[3]) == float(sc[1500])
+
+
+@pytest.mark.parametrize("shape,lengths,n_new", [
+    ((1, 16, 4, 64, 32, 32, 1200), [1000], 3),   # 4 kv heads x 2 tiles of 16 tokens, hd 64
+    ((1, 32, 8, 128, 32, 32, 1200), [1000], 2),  # 16 tiles per block
+    ((1, 8, 1, 64, 16, 16, 400), [1, 300, 2], 8),  # one tile per block, r 16
+])
+def test_layer_step_new_blocks_other_shapes(shape, lengths, n_new):
+    d = W.Dims(*shape)
+    x = make(d, lengths, 1, n_new, seed=sum(shape) + n_new)
+    inline_vs_oracle(d, x, 0, 16)
+
+
 def test_layer_step_bad_new_id():
     # A new id outside the pool is skipped and reported; the call's other results stand.
     d = W.Dims(1, 32, 8, 128, 32, 16, 2100)
