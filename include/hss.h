@@ -301,8 +301,8 @@ hss_status hss_select_rows(const float* scores, int32_t rows, int64_t num_blocks
  *                            bf16 ulp.
  *   scores, victims          outputs, as in hss_score_blocks / hss_rank_victims
  *   workspace                device, >= hss_layer_step_workspace_bytes(num_seqs) bytes,
- *                            4-byte aligned (8-byte aligned for the one-sequence ranking
- *                            above): the one-sequence ranking's call number and 32 KiB of
+ *                            4-byte aligned (16-byte aligned for the in-kernel ranking of
+ *                            at most 8 sequences above): that ranking's call number and 32 KiB of
  *                            tagged keys (33024 bytes), then the per-sequence completion
  *                            counters, so calls with different num_seqs may share one
  *                            workspace sized for the largest.  Zero all of it once

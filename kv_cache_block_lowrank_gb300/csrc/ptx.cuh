@@ -38,6 +38,13 @@ __device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gmem_src
                  : "memory");
 }
 
+// 4 bytes through L1 (read-only data).
+__device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)),
+                 "l"(gmem_src)
+                 : "memory");
+}
+
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }

@@ -427,7 +427,24 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
         }
         staged = true;
     };
-    if (INLINE && p.early) stage_issue();  // the previous kernel writes neither Q nor P
+    // Spread ranking: the call's offsets and its number (the word the previous call advanced)
+    // are copied into shared memory before any slot is requested (behind the slots' traffic
+    // their round trip took microseconds), by asynchronous copies that hold no registers;
+    // they are waited for with the queries' rows, or before this CTA's keys go out.
+    bool spread_issued = false;
+    auto spread_issue = [&]() {
+        spread_issued = true;
+        if (!p.spread) return;
+        uint32_t* tag_smem = reinterpret_cast<uint32_t*>(smem_dec + p.frag_bytes_cta) + p.todo_cap +
+                             kWarpsMax * kSpreadMaxCta;
+        if (static_cast<int>(threadIdx.x) <= p.num_seqs)
+            cp_async_4(tag_smem + 4 + threadIdx.x, p.seq_offsets + threadIdx.x);
+        if (threadIdx.x == 0) cp_async_16(tag_smem, p.counters);  // L2 only: the current word
+    };
+    if (INLINE && p.early) {
+        stage_issue();  // the previous kernel writes neither Q nor P
+        spread_issue();
+    }
 
     if (p.early && has_work) {
         // The previous kernel in the stream is this call's own projection, which writes only
@@ -456,6 +473,7 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
     // nowait: this lane's new id (lane < num_new <= 32); a warp waits before its first one.
     const int32_t my_new = nowait && lane < p.num_new ? __ldg(&p.new_ids[lane]) : -1;
     bool waited = !nowait;
+    if (!spread_issued) spread_issue();
 
     if constexpr (INLINE) {
         if (!staged) stage_issue();
@@ -788,7 +806,7 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
         // the ranks are a permutation, ordered by (key, position).
         uint32_t* ekey = reinterpret_cast<uint32_t*>(smem_dec + p.frag_bytes_cta);
         uint32_t* part = ekey + p.todo_cap;  // [warp][kSpreadMaxCta] partial counts, then
-        uint32_t* tag_smem = part + kWarpsMax * kSpreadMaxCta;  // this call's tag,
+        uint32_t* tag_smem = part + kWarpsMax * kSpreadMaxCta;  // the last call's number,
         int32_t* soff = reinterpret_cast<int32_t*>(tag_smem + 4);  // seq_offsets[0 .. S],
         uint8_t* eseq = reinterpret_cast<uint8_t*>(soff + kSpreadMaxSeqs + 1);  // entries' seqs
         const int S = p.num_seqs;
@@ -796,10 +814,8 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
         const int64_t cb = static_cast<int64_t>(blockIdx.x) * per_cta;
         int* epoch = p.counters;
         uint64_t* words = reinterpret_cast<uint64_t*>(p.counters + kSpreadWordsOffsetWords);
-        if (static_cast<int>(threadIdx.x) <= S) soff[threadIdx.x] = __ldg(&p.seq_offsets[threadIdx.x]);
-        if (threadIdx.x == 0)
-            *tag_smem = (static_cast<uint32_t>(ld_relaxed_gpu(epoch)) + 1u) & kSpreadTagMask;
-        __syncthreads();  // this CTA's keys, the tag and the offsets
+        cp_async_wait_all();  // the offsets and the call number
+        __syncthreads();  // this CTA's keys, the call number and the offsets
         const int64_t a = soff[0], b = soff[S];
         if (a < 0 || b < a || b > p.total || b - a > kSpreadMaxEntries) {
             // Offsets that do not describe at most 4096 of the scored entries: nothing is
@@ -825,7 +841,7 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
             grid_launch_dependents();
             return;
         }
-        const uint32_t tag = *tag_smem;
+        const uint32_t tag = (*tag_smem + 1u) & kSpreadTagMask;  // this call's number
         const int pos0 = static_cast<int>(eb - a);  // position of this CTA's first entry
         // (self-test: the withheld CTA, an index past the grid meaning its last one)
         const int withheld = p.withhold_cta < 0 ? -1
@@ -1093,7 +1109,7 @@ hss_status launch_score_decode(const ScoreArgs& a, cudaStream_t stream, const Fu
     p.spread = 0;
     if (fr != nullptr && fr->spread_region != nullptr && warps_per_cta == kWarpsMax &&
         a.num_seqs >= 1 && a.num_seqs <= kSpreadMaxSeqs && a.total <= kSpreadMaxEntries &&
-        (reinterpret_cast<uintptr_t>(fr->spread_region) & 7u) == 0 &&
+        (reinterpret_cast<uintptr_t>(fr->spread_region) & 15u) == 0 && p.frag_bytes_cta % 16 == 0 &&
         p.entries_per_warp * warps_per_cta <= kSpreadMaxCta) {
         // Spread ranking needs the whole grid resident at once (its CTAs wait for each other).
         const int todo_cap = static_cast<int>(p.entries_per_warp * warps_per_cta);
