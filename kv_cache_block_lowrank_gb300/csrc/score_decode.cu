@@ -136,12 +136,6 @@ __device__ __forceinline__ void sub_if_less(uint32_t& below, uint64_t w, uint64_
           "r"(static_cast<uint32_t>(we)), "r"(static_cast<uint32_t>(we >> 32)));
 }
 
-__device__ __forceinline__ int ld_relaxed_gpu(const int* addr) {
-    int v;
-    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
-    return v;
-}
-
 __device__ __forceinline__ uint64_t ld_relaxed_gpu_u64(const uint64_t* addr) {
     uint64_t v;
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(addr) : "memory");
