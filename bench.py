@@ -193,8 +193,8 @@ def measured_peaks():
 # dram__bytes_write.sum) from the ncu captures summarised in profiles/, or None when the
 # kernel has changed since its capture.
 TRAFFIC = {
-    "decode": (16882432 + 0, "profiles/score_decode_layer_step.md"),
-    "batched": (283580928 + 2741504, "profiles/score_decode_batched.md"),
+    "decode": (16886144 + 0, "profiles/score_decode_layer_step.md"),
+    "batched": (283582976 + 3016448, "profiles/score_decode_batched.md"),
     "prefill": (143540224, "profiles/score_tc_prefill.md"),
     # captured on a 40000-block launch; traffic grows with the blocks, so scaled to 4096
     "ingest": (round((1310970000 + 305094400) * 4096 / 40000),
