@@ -101,6 +101,7 @@ struct TcParams {
 struct Unit {
     int s, c, q;
     int64_t t;       // tile within the sequence
+    int64_t tiles;   // the sequence's tiles
     int64_t first;   // table index of the sequence's first block
     int64_t end;     // one past its last
     int64_t pair;    // (s, c, q) identity
@@ -120,6 +121,7 @@ __device__ __forceinline__ Unit decode_unit(int64_t u, int q, const TcParams& p,
     x.first = offs[lo];
     x.end = offs[lo + 1];
     const int64_t tiles = (x.end - x.first + p.bpt - 1) / p.bpt;
+    x.tiles = tiles;
     const int64_t local = u - units_before[lo];
     const int64_t c = local / tiles;
     x.t = local - c * tiles;
@@ -127,6 +129,28 @@ __device__ __forceinline__ Unit decode_unit(int64_t u, int q, const TcParams& p,
     x.q = q;
     x.pair = units_before[lo] + c * tiles;  // unique per (s, c); the slice is fixed per CTA
     return x;
+}
+
+// The unit after x (u + 1): the next tile, kv head or non-empty sequence, without
+// decode_unit's search and 64-bit divisions (the single MMA-issuing thread pays them per
+// tile otherwise).  Past the last unit it leaves x on the last sequence; nobody reads it.
+__device__ __forceinline__ void advance_unit(Unit& x, const TcParams& p,
+                                             const int64_t* units_before, const int32_t* offs) {
+    if (++x.t < x.tiles) return;
+    x.t = 0;
+    if (++x.c < p.nkv) {
+        x.pair += x.tiles;
+        return;
+    }
+    x.c = 0;
+    int s = x.s + 1;
+    if (s >= p.num_seqs) return;
+    while (s + 1 < p.num_seqs && units_before[s + 1] == units_before[s]) ++s;  // empty ones
+    x.s = s;
+    x.first = offs[s];
+    x.end = offs[s + 1];
+    x.tiles = (x.end - x.first + p.bpt - 1) / p.bpt;
+    x.pair = units_before[s];
 }
 
 __device__ __forceinline__ void atomic_max_f32(float* addr, float v) {
@@ -348,6 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                               : 0;
     const int nchunks = p.slice / kNChunk;
     const int elems_per_row = p.row_bytes / 2;
+    Unit first_unit{};
+    if (u_begin < u_end) first_unit = decode_unit(u_begin, q_slice, p, units_before, offs);
 
     if (warp == 0) {
         if (lane == 0) {
@@ -357,8 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0, b_empty_phase = 0, b_loads = 0;
             int64_t prev_pair = -1, issued = 0;
             bool ok = true;
-            for (int64_t u = u_begin; u < u_end && ok; ++u) {
-                const Unit x = decode_unit(u, q_slice, p, units_before, offs);
+            Unit x = first_unit;
+            for (int64_t u = u_begin; u < u_end && ok;
+                 ++u, advance_unit(x, p, units_before, offs)) {
                 if (x.pair != prev_pair) {
                     if (prev_pair >= 0) {
                         ok = mbar_wait(b_empty, b_empty_phase);
@@ -423,8 +450,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0, b_full_phase = 0;
             int64_t prev_pair = -1, it = 0;
             bool ok = true;
-            for (int64_t u = u_begin; u < u_end && ok; ++u) {
-                const Unit x = decode_unit(u, q_slice, p, units_before, offs);
+            Unit x = first_unit;
+            for (int64_t u = u_begin; u < u_end && ok;
+                 ++u, advance_unit(x, p, units_before, offs)) {
                 if (x.pair != prev_pair) {
                     if (prev_pair >= 0) umma_commit(b_empty);  // old slice free once MMAs finish
                     ok = mbar_wait(b_full, b_full_phase);
@@ -437,8 +465,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t a0 = smem_u32(sA + stage * p.a_stage_bytes);
-                const uint32_t b0 = smem_u32(sB);
+                // The descriptors' start-address field holds the byte address >> 4 (14 bits; the
+                // shared-memory window stays below 256 KiB), so stepping through the operands
+                // adds (offset >> 4) to a base descriptor: the single issuing thread spends a
+                // few instructions per MMA, not a descriptor build (a chunk is only K = r deep).
+                const uint64_t a_desc0 = smem_desc_kmajor(smem_u32(sA + stage * p.a_stage_bytes),
+                                                          p.row_bytes);
+                const uint64_t b_desc0 = smem_desc_kmajor(smem_u32(sB), p.row_bytes);
+                const uint32_t a_kc = (kTileTokens * p.row_bytes) >> 4;
+                const uint32_t b_kc = (p.slice * p.row_bytes) >> 4;
+                const uint32_t b_nc = (kNChunk * p.row_bytes) >> 4;
+                const int ksteps = elems_per_row / 16;
                 for (int nc = 0; nc < nchunks && ok; ++nc, ++it) {
                     const int acc = static_cast<int>(it & 1);
                     if (!mbar_wait(&t_empty[acc], static_cast<uint32_t>(((it >> 1) & 1) ^ 1))) {
@@ -447,15 +484,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after_sync();
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kNChunk);
-                    for (int kc = 0; kc < p.kchunks; ++kc) {
-                        for (int ks = 0; ks < elems_per_row / 16; ++ks) {
-                            const uint64_t ad = smem_desc_kmajor(
-                                a0 + kc * (kTileTokens * p.row_bytes) + ks * 32, p.row_bytes);
-                            const uint64_t bd = smem_desc_kmajor(
-                                b0 + kc * (p.slice * p.row_bytes) + nc * (kNChunk * p.row_bytes) +
-                                    ks * 32,
-                                p.row_bytes);
-                            umma_bf16(d_tmem, ad, bd, idesc, (kc | ks) != 0 ? 1u : 0u);
+                    uint64_t ad_kc = a_desc0, bd_kc = b_desc0 + nc * b_nc;
+                    for (int kc = 0; kc < p.kchunks; ++kc, ad_kc += a_kc, bd_kc += b_kc) {
+                        for (int ks = 0; ks < ksteps; ++ks) {
+                            // ks * 32 bytes along K inside the swizzled rows: + 2 per step
+                            umma_bf16(d_tmem, ad_kc + 2 * ks, bd_kc + 2 * ks, idesc,
+                                      (kc | ks) != 0 ? 1u : 0u);
                         }
                     }
                     umma_commit(&t_full[acc]);
@@ -479,8 +513,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int token = quarter * 32 + lane;
         int64_t it = 0;  // global chunk counter, shared numbering with the MMA warp
         bool ok = true;
+        // (masked mode and per-row mode with g <= 2: each unit decoded afresh, their
+        // epilogues have no registers to spare)
+        Unit x = first_unit;
         for (int64_t u = u_begin; u < u_end && ok; ++u) {
-            const Unit x = decode_unit(u, q_slice, p, units_before, offs);
+            if constexpr ((ROWG > 0 && ROWG < 4) || MASKED) {
+                x = decode_unit(u, q_slice, p, units_before, offs);
+            } else if (u > u_begin) {
+                advance_unit(x, p, units_before, offs);
+            }
             float run = -INFINITY;
             bool any = false;
             // This thread's token position; with masks, the token may be hidden (past the

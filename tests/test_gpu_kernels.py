@@ -253,6 +253,8 @@ def test_rank_victims_all_equal():
     (32, 2, 16, 16, 70, [11]),           # g = 16, r = 16 (32-byte swizzle), 1120 vectors
     (32, 8, 32, 16, 1, [300]),           # the decode shape forced onto the tensor-core path
     (64, 8, 64, 16, 512, [24]),          # the prefill chunk shape, few blocks
+    (16, 4, 32, 16, 3, [5, 0, 0, 40, 0, 17, 0]),   # empty sequences between and after
+    (32, 8, 64, 16, 2, [1] * 30 + [0] * 3 + [100]),  # a CTA's units span many sequences
 ])
 def test_score_tcgen05(nq, nkv, r, bs, rows, lengths):
     g = gen(nq * 3 + nkv + r + bs + rows)
