@@ -229,14 +229,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * r);
-                const uint32_t a0 = smem_u32(sA + stage * stage_bytes);
-                const uint32_t b0 = smem_u32(sB);
-                for (int c = 0; c < kchunks; ++c) {
-                    for (int s = 0; s < kChunkElems / 16; ++s) {
-                        const uint64_t ad = smem_desc_kmajor(a0 + c * kChunkBytes + s * 32, 128);
-                        const uint64_t bd = smem_desc_kmajor(b0 + c * r * 128 + s * 32, 128);
-                        umma_bf16(d_tmem, ad, bd, idesc, (c | s) != 0 ? 1u : 0u);
-                    }
+                // Descriptors step by (offset >> 4) from a base (the start-address field holds
+                // the address >> 4 and never carries below 256 KiB).
+                uint64_t ad = smem_desc_kmajor(smem_u32(sA + stage * stage_bytes), 128);
+                uint64_t bd = smem_desc_kmajor(smem_u32(sB), 128);
+                for (int c = 0; c < kchunks; ++c, ad += kChunkBytes >> 4, bd += (r * 128) >> 4) {
+#pragma unroll
+                    for (int s = 0; s < kChunkElems / 16; ++s)  // 32 bytes along K per step
+                        umma_bf16(d_tmem, ad + 2 * s, bd + 2 * s, idesc, (c | s) != 0 ? 1u : 0u);
                 }
                 umma_commit(&empty[stage]);  // smem stage free once these MMAs have read it
                 umma_commit(&tfull[acc]);    // accumulator ready for the epilogue
@@ -312,6 +312,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
             const int acc = static_cast<int>(it & 1);
             const uint32_t acc_phase = static_cast<uint32_t>((it >> 1) & 1);
+            // The row's slot or block id is requested before the wait for the accumulator, so
+            // the lookup's latency overlaps it; the destination is formed after.
+            const bool second = tile >= p.seg[0].tiles;
+            const ProjSegment& sg = second ? p.seg[1] : p.seg[0];
+            const int64_t m = (second ? tile - p.seg[0].tiles : tile) * kBM + row_in_tile;
+            const bool have = m < sg.num_rows;
+            int64_t look = -1;  // the token's slot, or the block's id
+            int h = 0, t = 0, rem = 0;
+            if (have) {
+                if (sg.slots != nullptr) {
+                    // Row m = (token i, kv head h); the token's slot names block and position.
+                    const int64_t i = m / p.num_kv_heads;
+                    h = static_cast<int>(m - i * p.num_kv_heads);
+                    look = sg.slots[i];
+                } else if (sg.block_ids != nullptr) {
+                    const int64_t i = m / rows_per_block;
+                    rem = static_cast<int>(m - i * rows_per_block);
+                    t = rem / p.num_kv_heads;
+                    h = rem - t * p.num_kv_heads;
+                    look = sg.block_ids[i];
+                }
+            }
             const bool ok = mbar_wait(&tfull[acc], acc_phase);
             if (__any_sync(0xffffffffu, !ok) || *(volatile int*)abort_flag) {
                 if (lane == 0) {
@@ -321,32 +343,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after_sync();
-            const bool second = tile >= p.seg[0].tiles;
-            const ProjSegment& sg = second ? p.seg[1] : p.seg[0];
-            const int64_t m = (second ? tile - p.seg[0].tiles : tile) * kBM + row_in_tile;
             uint16_t* dst = nullptr;
-            if (m < sg.num_rows) {
+            if (have) {
                 if (sg.slots != nullptr) {
-                    // Row m = (token i, kv head h); the token's slot names block and position.
-                    const int64_t i = m / p.num_kv_heads;
-                    const int h = static_cast<int>(m - i * p.num_kv_heads);
-                    const int64_t sl = sg.slots[i];
+                    const int64_t sl = look;
                     if (sl >= 0 && sl < p.max_blocks * p.block_size) {
                         const int64_t blk = sl / p.block_size;
-                        const int t = static_cast<int>(sl - blk * p.block_size);
+                        const int tt = static_cast<int>(sl - blk * p.block_size);
                         dst = sg.out + (((p.layer_slots + blk) * p.num_kv_heads + h) *
-                                            p.block_size + t) * static_cast<int64_t>(r);
+                                            p.block_size + tt) * static_cast<int64_t>(r);
                     } else if (sl >= 0 && h == 0) {
                         raise_error(p.dev_status, p.lib_error, HSS_ERR_OUT_OF_RANGE);
                     }
                 } else if (sg.block_ids == nullptr) {
                     dst = sg.out + m * r;
                 } else {
-                    const int64_t i = m / rows_per_block;
-                    const int rem = static_cast<int>(m - i * rows_per_block);
-                    const int t = rem / p.num_kv_heads;
-                    const int h = rem - t * p.num_kv_heads;
-                    const int64_t id = sg.block_ids[i];
+                    const int64_t id = look;
                     if (id >= 0 && id < p.max_blocks) {
                         dst = sg.out + (((p.layer_slots + id) * p.num_kv_heads + h) * p.block_size +
                                        t) * static_cast<int64_t>(r);
