@@ -524,6 +524,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             float run = -INFINITY;
             bool any = false;
+            // Per-row mode: this lane's block and whether its id is valid, looked up once per
+            // unit (before the first chunk's wait, which hides the load).
+            int64_t row_st = 0, row_ee = 0;
+            bool row_ok = false;
+            if constexpr (ROWG > 0) {
+                const int64_t e = x.first + x.t * p.bpt + token / p.bs;
+                row_ok = e < x.end;
+                if (row_ok) {
+                    const int64_t id = p.table[e];
+                    row_ok = id >= 0 && id < p.max_blocks;
+                    if (!row_ok && x.c == 0 && x.q == 0 && (lane & (p.bs - 1)) == 0)
+                        raise_error(p.dev_status, p.lib_error, HSS_ERR_OUT_OF_RANGE);
+                }
+                row_st = x.end - x.first;
+                row_ee = e - x.first;
+            }
             // This thread's token position; with masks, the token may be hidden (past the
             // context) or visible only to query rows from some row on (causal).
             bool tok_ok = true;
@@ -579,17 +595,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&t_empty[acc]);
                     if (valid > 0) {
-                        const int blk = token / p.bs;
-                        const int64_t e = x.first + x.t * p.bpt + blk;
-                        bool e_ok = e < x.end;
-                        if (e_ok) {
-                            const int64_t id = p.table[e];
-                            e_ok = id >= 0 && id < p.max_blocks;
-                            if (!e_ok && x.c == 0 && x.q == 0 && nc == 0 &&
-                                (lane & (p.bs - 1)) == 0)
-                                raise_error(p.dev_status, p.lib_error, HSS_ERR_OUT_OF_RANGE);
-                        }
-                        const int64_t st = x.end - x.first, ee = e - x.first;
+                        const bool e_ok = row_ok;
+                        const int64_t st = row_st, ee = row_ee;
                         if (p.bs == 16)
                             scatter_rows<ROWG, 16>(xr, v0, lane, p.rows, p.scores, st, ee, e_ok);
                         else
@@ -611,17 +618,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&t_empty[acc]);
                     if (valid > 0) {
-                        const int blk = token / p.bs;
-                        const int64_t e = x.first + x.t * p.bpt + blk;
-                        bool e_ok = e < x.end;
-                        if (e_ok) {
-                            const int64_t id = p.table[e];
-                            e_ok = id >= 0 && id < p.max_blocks;
-                            if (!e_ok && x.c == 0 && x.q == 0 && nc == 0 &&
-                                (lane & (p.bs - 1)) == 0)
-                                raise_error(p.dev_status, p.lib_error, HSS_ERR_OUT_OF_RANGE);
-                        }
-                        const int64_t st = x.end - x.first, ee = e - x.first;
+                        const bool e_ok = row_ok;
+                        const int64_t st = row_st, ee = row_ee;
                         if (p.bs == 16) {
                             rows_to_scores<ROWG, 16, 0, 32>(v, valid, v0, lane, p.rows, p.scores, st, ee, e_ok);
                             if (valid > 32) rows_to_scores<ROWG, 16, 32, 32>(v, valid - 32, v0 + 32, lane, p.rows, p.scores, st, ee, e_ok);
