@@ -524,22 +524,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             float run = -INFINITY;
             bool any = false;
-            // Per-row mode: this lane's block and whether its id is valid, looked up once per
-            // unit (before the first chunk's wait, which hides the load).
-            int64_t row_st = 0, row_ee = 0;
+            // This lane's block and whether its id is valid, looked up once per unit, before
+            // the first chunk's wait (which hides the load).
+            const int64_t blk_e = x.first + x.t * p.bpt + token / p.bs;
+            const bool blk_in = blk_e < x.end;
             bool row_ok = false;
-            if constexpr (ROWG > 0) {
-                const int64_t e = x.first + x.t * p.bpt + token / p.bs;
-                row_ok = e < x.end;
-                if (row_ok) {
-                    const int64_t id = p.table[e];
-                    row_ok = id >= 0 && id < p.max_blocks;
-                    if (!row_ok && x.c == 0 && x.q == 0 && (lane & (p.bs - 1)) == 0)
-                        raise_error(p.dev_status, p.lib_error, HSS_ERR_OUT_OF_RANGE);
-                }
-                row_st = x.end - x.first;
-                row_ee = e - x.first;
+            if (blk_in) {
+                const int64_t id = p.table[blk_e];
+                row_ok = id >= 0 && id < p.max_blocks;
+                if (!row_ok && x.c == 0 && x.q == 0 && (lane & (p.bs - 1)) == 0)
+                    raise_error(p.dev_status, p.lib_error, HSS_ERR_OUT_OF_RANGE);
             }
+            const int64_t row_st = x.end - x.first, row_ee = blk_e - x.first;
             // This thread's token position; with masks, the token may be hidden (past the
             // context) or visible only to query rows from some row on (causal).
             bool tok_ok = true;
@@ -688,20 +684,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Max over the block's tokens: block_size consecutive lanes.
             for (int off = p.bs >> 1; off > 0; off >>= 1)
                 run = fmaxf(run, __shfl_xor_sync(0xffffffffu, run, off));
-            if ((lane & (p.bs - 1)) == 0) {
-                const int blk = token / p.bs;
-                const int64_t e = x.first + x.t * p.bpt + blk;
-                if (e < x.end) {
-                    const int64_t id = p.table[e];
-                    if (id >= 0 && id < p.max_blocks) {
-                        atomic_max_f32(p.scores + e, run);
-                    } else {
-                        atomic_max_f32(p.scores + e, INFINITY);
-                        if (x.c == 0 && x.q == 0)
-                            raise_error(p.dev_status, p.lib_error, HSS_ERR_OUT_OF_RANGE);
-                    }
-                }
-            }
+            if ((lane & (p.bs - 1)) == 0 && blk_in)
+                atomic_max_f32(p.scores + blk_e, row_ok ? run : INFINITY);
         }
         if (!ok && lane == 0) {
             raise_error(p.dev_status, p.lib_error, HSS_ERR_DEVICE_TIMEOUT);
