@@ -195,12 +195,12 @@ def measured_peaks():
 TRAFFIC = {
     "decode": (16886144 + 0, "profiles/score_decode_layer_step.md"),
     "batched": (283582976 + 3016448, "profiles/score_decode_batched.md"),
-    "prefill": (139981056 + 3294976, "profiles/score_tc_prefill.md"),
+    "prefill": (139942144 + 3391488, "profiles/score_tc_prefill.md"),
     # captured on a 40000-block launch; traffic grows with the blocks, so scaled to 4096
     "ingest": (round((1311202000 + 305371392) * 4096 / 40000),
                "profiles/project_ingest_40000_blocks.md, scaled from 40000 to 4096 blocks"),
     "ingest_tokens": (134825472 + 112101120, "profiles/project_tokens_65536.md"),
-    "prefill_rows": (156995840 + 3903232, "profiles/score_tc_prefill_rows.md"),
+    "prefill_rows": (157091328 + 3819520, "profiles/score_tc_prefill_rows.md"),
 }
 
 
