@@ -547,8 +547,14 @@ hss_status launch_project2(const ProjectArgs& a0, const ProjectArgs* a1, cudaStr
     p.lib_error = dev->error_word;
     const int64_t num_tiles = p.seg[0].tiles + p.seg[1].tiles;
     const int grid = static_cast<int>(std::min<int64_t>(num_tiles, dev->num_sms));
-    const int stages = L.stages;
-    if (launch_pdl(project_kernel, dim3(grid), dim3(kThreads), L.total_bytes, stream, map0, map1,
+    // A CTA takes at most ceil(num_tiles / grid) tiles: more stages than that would only hold
+    // shared memory.  With one tile (a decode step's new block) two stages need 75 KiB instead
+    // of 206, so the CTA fits beside a decode scorer's CTA and can do its set-up while that
+    // grid finishes.
+    const int64_t per_cta = (num_tiles + grid - 1) / grid;
+    const int stages = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(L.stages, per_cta)));
+    const int smem_bytes = L.total_bytes - (L.stages - stages) * L.stage_bytes;
+    if (launch_pdl(project_kernel, dim3(grid), dim3(kThreads), smem_bytes, stream, map0, map1,
                    p, stages) != cudaSuccess)
         return HSS_ERR_CUDA;
     return HSS_OK;

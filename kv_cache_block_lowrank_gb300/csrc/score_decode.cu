@@ -461,8 +461,8 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
     }
     const bool nowait = INLINE && p.nowait != 0;
     if (!nowait) grid_dependency_wait();
-    // Spread ranking waits for every CTA of this grid: the next kernel may not take their
-    // places (it is let in once a CTA has seen every CTA's keys).
+    // Spread ranking waits for every CTA of this grid: the next kernel is let in only once a
+    // CTA has published its keys (all CTAs are then resident, so it cannot take their places).
     if (!p.spread) grid_launch_dependents();
     // nowait: this lane's new id (lane < num_new <= 32); a warp waits before its first one.
     const int32_t my_new = nowait && lane < p.num_new ? __ldg(&p.new_ids[lane]) : -1;
@@ -850,6 +850,9 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
                                    (static_cast<uint64_t>(tag) << 35) |
                                        (static_cast<uint64_t>(se) << 32) | ekey[eb - cb + threadIdx.x]);
         }
+        // Every CTA that gets here is resident and has published (or holds no entry): the next
+        // kernel may take free places now; it cannot take ours.
+        grid_launch_dependents();
         // Gather every word, counting as they arrive; each warp leaves its count of each of
         // the CTA's entries in `part` (no atomics).
         const bool ok = cnt <= 8
@@ -859,7 +862,6 @@ __global__ void __launch_bounds__(kWarpsMax * 32, 2) score_decode_kernel(const D
                                pos0, cnt, part + warp * kSpreadMaxCta);
         if (!ok && lane == 0) raise_error(p.dev_status, p.lib_error, HSS_ERR_DEVICE_TIMEOUT);
         __syncthreads();  // every thread has seen every word; the counts and eseq are set
-        grid_launch_dependents();
         // Every CTA has published, so every CTA has read the tag: the CTA holding the call's
         // first entry advances the call number for the next call.
         if (threadIdx.x == 0 && static_cast<int64_t>(blockIdx.x) == a / per_cta)
