@@ -193,7 +193,7 @@ def measured_peaks():
 # dram__bytes_write.sum) from the ncu captures summarised in profiles/, or None when the
 # kernel has changed since its capture.
 TRAFFIC = {
-    "decode": (16886144 + 0, "profiles/score_decode_layer_step.md"),
+    "decode": (16886656 + 0, "profiles/score_decode_layer_step.md"),
     "batched": (283582976 + 3016448, "profiles/score_decode_batched.md"),
     "prefill": (139942144 + 3391488, "profiles/score_tc_prefill.md"),
     # captured on a 40000-block launch; traffic grows with the blocks, so scaled to 4096
