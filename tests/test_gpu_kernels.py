@@ -91,6 +91,34 @@ def test_project_kv_blocks(nkv, bs, r, n):
     assert (got[:layer] == SENTINEL).all(), "wrote another layer"
 
 
+@pytest.mark.parametrize("per_cta", [2, 3, 5])
+def test_project_kv_blocks_stage_rings(per_cta):
+    # The projection's ring has as many stages as a CTA has tiles (at least two): 152 * (k - 1)
+    # + 1 one-tile blocks give some CTAs k tiles, so rings of 2, 3 and 5 stages wrap.
+    g = gen(300 + per_cta)
+    n = 152 * (per_cta - 1) + 1
+    B, hd, r = n + 50, 128, 32
+    d = dims(L=1, nq=32, nkv=8, hd=hd, r=r, bs=16, B=B)
+    P = W.projection(g, hd, r)
+    K = W.bf16_normal(g, (n, 16, 8, hd))
+    ids = torch.randperm(B, generator=g)[:n].to(torch.int32)
+    A = torch.empty(d.a_g_shape, dtype=torch.bfloat16, device=DEV)
+    A.view(torch.int16).fill_(SENTINEL)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    hss.hss_project_kv_blocks(d, P.to(DEV), K.to(DEV), 0, ids.to(DEV), n, A, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = np.zeros((1, B, 8, 16, r), dtype=np.uint16)
+    oracle.project_kv_blocks(bits(P), bits(K), 0, ids.numpy(), ref, nthreads=8)
+    got = bits(A)
+    scale = abs_sum_scale(bits(K), bits(P)).transpose(0, 2, 1, 3)
+    assert_bf16_within_ulp(got[0][ids.numpy()], ref[0][ids.numpy()], what="A_g slots",
+                           scale=scale, n_terms=hd)
+    untouched = np.ones(B, dtype=bool)
+    untouched[ids.numpy()] = False
+    assert (got[0][untouched] == SENTINEL).all()
+
+
 def test_project_kv_out_of_range_ids_are_skipped_and_reported():
     g = gen(77)
     d = dims(L=2, nq=8, nkv=8, hd=128, r=32, bs=16, B=16)
