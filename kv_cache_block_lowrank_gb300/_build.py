@@ -13,9 +13,10 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhss.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["hss_api.cu", "project_tc.cu", "score_decode.cu", "score_tc.cu", "rank.cu",
-           "no_alloc.cu", "selftest.cu"]
-HEADERS = ["ptx.cuh", "internal.h", "rank_device.cuh"]
+SOURCES = ["hss_api.cu", "project_tc.cu", "score_decode.cu", "score_decode_k1.cu",
+           "score_decode_k2.cu", "score_decode_k4.cu", "score_decode_k8.cu", "score_tc.cu",
+           "rank.cu", "no_alloc.cu", "selftest.cu"]
+HEADERS = ["ptx.cuh", "internal.h", "rank_device.cuh", "score_decode_kernel.cuh"]
 
 
 def nvcc() -> str:
