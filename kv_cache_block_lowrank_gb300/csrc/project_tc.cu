@@ -458,7 +458,7 @@ struct MapCacheEntry {
     int32_t head_dim = 0;
     CUtensorMap map;
 };
-constexpr int kMapCache = 8;
+constexpr int kMapCache = 64;  // e.g. a decode step: 32 layers, a query and a key buffer each
 MapCacheEntry g_map_cache[kMapCache];
 int g_map_next = 0;
 std::mutex g_map_mu;

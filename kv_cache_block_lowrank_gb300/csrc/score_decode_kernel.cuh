@@ -977,9 +977,20 @@ hss_status launch_t(const DecodeParams& p, int warps_per_cta, int smem, int grid
                     cudaStream_t stream) {
     auto k = kernel_for<KSTEPS, NT>(p);
     if (smem > 48 * 1024) {
-        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-            cudaSuccess)
-            return HSS_ERR_CUDA;
+        // The largest dynamic shared memory already allowed, per kernel of kernel_for and
+        // device: the attribute call is made only when a launch needs more (a host-side
+        // saving on every layer call).
+        static std::atomic<int> allowed[4][64];
+        const int which = p.Q != nullptr ? (p.tma_buf_off != 0 ? 3 : 0)
+                          : (p.ctx_len != nullptr || p.row_pos0 != nullptr) ? 1 : 2;
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return HSS_ERR_CUDA;
+        if (allowed[which][dev].load(std::memory_order_relaxed) < smem) {
+            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+                cudaSuccess)
+                return HSS_ERR_CUDA;
+            allowed[which][dev].store(smem, std::memory_order_relaxed);
+        }
     }
     if (launch_pdl(k, dim3(grid), dim3(warps_per_cta * 32), smem, stream, p) != cudaSuccess)
         return HSS_ERR_CUDA;
