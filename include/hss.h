@@ -325,6 +325,41 @@ hss_status hss_layer_step(const hss_dims* dims, const uint16_t* P, const uint16_
                           int32_t* dev_status, void* stream);
 
 /*
+ * hss_layer_step with the arguments that stay the same from call to call bound once in a
+ * struct (a serving loop's layer calls differ only in the layer, the new key blocks, the
+ * queries, the outputs and the stream): one call is exactly
+ *   hss_layer_step(&args->dims, args->P, K_new, args->new_ids, args->num_new, Q,
+ *                  args->rows_per_seq, args->Qp, args->A_g, layer, args->block_table,
+ *                  args->seq_offsets, args->num_seqs, args->total_blocks, scores, args->k,
+ *                  victims, args->workspace, args->workspace_bytes, args->dev_status, stream)
+ * with every argument's meaning, layout, ownership and error as there; the struct is read
+ * during the call only (the caller keeps it).  A calling convention of this library (the
+ * pages have no counterpart): fewer arguments to marshal per call for bindings whose
+ * per-argument cost shows beside a 10 us layer call.  HSS_ERR_NULL_POINTER if args is NULL.
+ */
+typedef struct hss_layer_step_args {
+    hss_dims dims;
+    const uint16_t* P;
+    const int32_t* new_ids;
+    int64_t num_new;
+    int32_t rows_per_seq;
+    uint16_t* Qp;
+    uint16_t* A_g;
+    const int32_t* block_table;
+    const int32_t* seq_offsets;
+    int32_t num_seqs;
+    int64_t total_blocks;
+    int32_t k;
+    void* workspace;
+    size_t workspace_bytes;
+    int32_t* dev_status;
+} hss_layer_step_args;
+
+hss_status hss_layer_step_bound(const hss_layer_step_args* args, int32_t layer,
+                                const uint16_t* K_new, const uint16_t* Q, float* scores,
+                                int32_t* victims, void* stream);
+
+/*
  * hss_layer_step for callers that cannot allocate device memory.  (The predictor pages have
  * no counterpart: this is a calling convention of this library.)
  *

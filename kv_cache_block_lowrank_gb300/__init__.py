@@ -43,6 +43,7 @@ EXPORTED = (
     "hss_score_blocks_masked",
     "hss_layer_step_static_max_seqs", "hss_write_kv_tokens", "hss_score_rows",
     "hss_select_rows", "hss_self_test_wait_timeout", "hss_self_test_spread_wait",
+    "hss_layer_step_bound",
 )
 
 
@@ -131,6 +132,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.hss_layer_step.restype = i32
     lib.hss_layer_step.argtypes = [dp, vp, vp, vp, i64, vp, i32, vp, vp, i32, vp, vp, i32, i64,
                                    vp, i32, vp, vp, sz, vp, vp]
+    lib.hss_layer_step_bound.restype = i32
+    lib.hss_layer_step_bound.argtypes = [ctypes.POINTER(hss_layer_step_args), i32, vp, vp, vp,
+                                         vp, vp]
     _lib = lib
     return lib
 
@@ -277,36 +281,53 @@ def hss_layer_step(dims, P, K_new, new_ids, num_new: int, Q, rows_per_seq: int, 
     _check(st, "hss_layer_step")
 
 
+class hss_layer_step_args(ctypes.Structure):
+    """The bound arguments of hss_layer_step_bound (hss_layer_step_args in hss.h)."""
+
+    _fields_ = [
+        ("dims", hss_dims),
+        ("P", ctypes.c_void_p),
+        ("new_ids", ctypes.c_void_p),
+        ("num_new", ctypes.c_int64),
+        ("rows_per_seq", ctypes.c_int32),
+        ("Qp", ctypes.c_void_p),
+        ("A_g", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p),
+        ("seq_offsets", ctypes.c_void_p),
+        ("num_seqs", ctypes.c_int32),
+        ("total_blocks", ctypes.c_int64),
+        ("k", ctypes.c_int32),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+        ("dev_status", ctypes.c_void_p),
+    ]
+
+
 class LayerStep:
     """hss_layer_step with the arguments that stay the same from call to call bound once.
 
     A serving loop makes one layer call per layer and step with the same dims, P, A_g,
-    block table, offsets, workspace and sizes; binding them here leaves only the per-call
-    ones (layer, the new key blocks, the queries, the score and victim buffers, the stream)
-    to marshal.  Tensors or integer device addresses are accepted for those; the call is
-    exactly hss_layer_step (same C entry point, same arguments).
+    block table, offsets, workspace and sizes; they are bound once in an
+    hss_layer_step_args struct and each call passes only the per-call ones (layer, the new
+    key blocks, the queries, the score and victim buffers, the stream) to
+    hss_layer_step_bound, which is exactly hss_layer_step.  Tensors or integer device
+    addresses are accepted for those.
     """
 
     def __init__(self, dims, P, new_ids, num_new: int, rows_per_seq: int, Qp, A_g,
                  block_table, seq_offsets, num_seqs: int, total_blocks: int, k: int,
                  workspace, workspace_bytes: int, dev_status=None):
-        vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
-        self._fn = load().hss_layer_step
-        self._dims = hss_dims.of(dims)  # kept alive: the call passes its address
-        self._head = (ctypes.byref(self._dims), vp(_ptr(P)))
-        self._mid1 = (vp(_ptr(new_ids)), i64(int(num_new)))
-        self._mid2 = (i32(int(rows_per_seq)), vp(_ptr(Qp)), vp(_ptr(A_g)))
-        self._mid3 = (vp(_ptr(block_table)), vp(_ptr(seq_offsets)), i32(int(num_seqs)),
-                      i64(int(total_blocks)))
-        self._k = i32(int(k))
-        self._ws = (vp(_ptr(workspace)), sz(int(workspace_bytes)))
-        self._status = vp(_ptr(dev_status))
+        self._fn = load().hss_layer_step_bound
+        self._args = hss_layer_step_args(
+            hss_dims.of(dims), _ptr(P), _ptr(new_ids), int(num_new), int(rows_per_seq),
+            _ptr(Qp), _ptr(A_g), _ptr(block_table), _ptr(seq_offsets), int(num_seqs),
+            int(total_blocks), int(k), _ptr(workspace), int(workspace_bytes), _ptr(dev_status))
+        self._ref = ctypes.byref(self._args)  # kept alive with the struct
 
     def __call__(self, layer: int, K_new, Q, scores, victims, stream=None) -> None:
-        st = self._fn(*self._head, _ptr(K_new), *self._mid1, _ptr(Q), *self._mid2, int(layer),
-                      *self._mid3, _ptr(scores), self._k, _ptr(victims), *self._ws,
-                      self._status, _stream(stream))
-        _check(st, "hss_layer_step")
+        st = self._fn(self._ref, int(layer), _ptr(K_new), _ptr(Q), _ptr(scores), _ptr(victims),
+                      _stream(stream))
+        _check(st, "hss_layer_step_bound")
 
 
 def hss_layer_step_static_max_seqs() -> int:

@@ -389,6 +389,17 @@ hss_status hss_layer_step(const hss_dims* dims, const uint16_t* P, const uint16_
     return HSS_OK;
 }
 
+hss_status hss_layer_step_bound(const hss_layer_step_args* args, int32_t layer,
+                                const uint16_t* K_new, const uint16_t* Q, float* scores,
+                                int32_t* victims, void* stream) {
+    if (args == nullptr) return HSS_ERR_NULL_POINTER;
+    return hss_layer_step(&args->dims, args->P, K_new, args->new_ids, args->num_new, Q,
+                          args->rows_per_seq, args->Qp, args->A_g, layer, args->block_table,
+                          args->seq_offsets, args->num_seqs, args->total_blocks, scores, args->k,
+                          victims, args->workspace, args->workspace_bytes, args->dev_status,
+                          stream);
+}
+
 hss_status hss_self_test_spread_wait(const hss_dims* dims, const uint16_t* P, const uint16_t* Q,
                                      uint16_t* A_g, int32_t layer, const int32_t* block_table,
                                      const int32_t* seq_offsets, int64_t total_blocks,

@@ -45,6 +45,34 @@ def test_dims_struct_layout():
     assert hss.hss_dims.max_blocks.offset == 24
 
 
+def test_layer_step_args_struct_layout(tmp_path):
+    # The binding's struct against the header's, field by field, as the C compiler lays it out.
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = [f for f, _ in hss.hss_layer_step_args._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "hss.h"\nint main(void) {\n'
+                   '  printf("%zu\\n", sizeof(hss_layer_step_args));\n' +
+                   "".join(f'  printf("%zu\\n", offsetof(hss_layer_step_args, {f}));\n'
+                           for f in fields) + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    want = [ctypes.sizeof(hss.hss_layer_step_args)] + [
+        getattr(hss.hss_layer_step_args, f).offset for f in fields]
+    assert got == want
+
+
+def test_layer_step_bound_null_args(lib):
+    st = lib.hss_layer_step_bound(None, 0, None, None, None, None, None)
+    assert st == hss.HSS_ERR_NULL_POINTER
+
+
 D = dict(num_layers=32, num_q_heads=32, num_kv_heads=8, head_dim=128, r=32, block_size=16,
          max_blocks=2048)
 
