@@ -89,7 +89,7 @@ struct ProjParams {
     int32_t* lib_error;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     project_kernel(const __grid_constant__ CUtensorMap tmap_x0,
                    const __grid_constant__ CUtensorMap tmap_x1, const ProjParams p,
                    const int stages) {
@@ -546,13 +546,14 @@ hss_status launch_project2(const ProjectArgs& a0, const ProjectArgs* a1, cudaStr
     p.dev_status = kv != nullptr ? kv->dev_status : nullptr;
     p.lib_error = dev->error_word;
     const int64_t num_tiles = p.seg[0].tiles + p.seg[1].tiles;
-    const int grid = static_cast<int>(std::min<int64_t>(num_tiles, dev->num_sms));
+    const int grid = static_cast<int>(std::min<int64_t>(num_tiles, 2 * dev->num_sms));
     // A CTA takes at most ceil(num_tiles / grid) tiles: more stages than that would only hold
     // shared memory.  With one tile (a decode step's new block) two stages need 75 KiB instead
     // of 206, so the CTA fits beside a decode scorer's CTA and can do its set-up while that
-    // grid finishes.
+    // grid finishes.  At most three stages: two CTAs per SM.
     const int64_t per_cta = (num_tiles + grid - 1) / grid;
-    const int stages = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(L.stages, per_cta)));
+    const int stages = static_cast<int>(
+        std::max<int64_t>(2, std::min<int64_t>(std::min(L.stages, 3), per_cta)));
     const int smem_bytes = L.total_bytes - (L.stages - stages) * L.stage_bytes;
     if (launch_pdl(project_kernel, dim3(grid), dim3(kThreads), smem_bytes, stream, map0, map1,
                    p, stages) != cudaSuccess)
