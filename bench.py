@@ -197,9 +197,9 @@ TRAFFIC = {
     "batched": (283582976 + 3016448, "profiles/score_decode_batched.md"),
     "prefill": (139942144 + 3391488, "profiles/score_tc_prefill.md"),
     # captured on a 40000-block launch; traffic grows with the blocks, so scaled to 4096
-    "ingest": (round((1311202000 + 305371392) * 4096 / 40000),
+    "ingest": (round((1310975000 + 303530240) * 4096 / 40000),
                "profiles/project_ingest_40000_blocks.md, scaled from 40000 to 4096 blocks"),
-    "ingest_tokens": (134825472 + 112101120, "profiles/project_tokens_65536.md"),
+    "ingest_tokens": (134840576 + 112052480, "profiles/project_tokens_65536.md"),
     "prefill_rows": (157091328 + 3819520, "profiles/score_tc_prefill_rows.md"),
 }
 
